@@ -1,0 +1,129 @@
+"""Seeded synthetic workloads: shapes, seeds and value distributions only.
+
+This module holds none of the attention arithmetic.  Both the CUDA path (via
+the tests and the benchmark) and the float64 oracle are fed from here; neither
+side generates its own inputs.
+
+The five workloads are the ones the attention path is specified on:
+
+* ``tiny_fp32_stack``  -- batch 1, prefill T=64, 4 layers, fp32.  Layer types are
+  run as [S, F, S, F] with the last two shared (S reads 0, F reads 1); the
+  literal [S, S, S, F] would route the full tail layer to a sliding source of
+  another head width, which the same-type rule forbids.
+* ``prefill_bf16``     -- batch 1, T=2048, one sliding and one full layer.
+* ``decode_bf16``      -- batch 64, one new token each, KV lengths U[1024, 8192].
+* ``stack42_bf16``     -- 42 layers (5 sliding : 1 full, last 18 shared), batch 8,
+  prefill T=4096 then 128 decode steps.
+* ``longctx_decode_bf16`` -- batch 4, KV length 131072 on the full layer plus a
+  sliding layer.
+
+Values: q/k/v and cache contents ~ N(0, 1); norm weights ~ 1 + 0.1 N(0, 1)
+(float32).  bf16 workloads round the float32 draws to bf16 (torch's RNE cast).
+"""
+
+from __future__ import annotations
+
+import torch
+
+SLIDING, FULL = 0, 1
+F32, BF16 = 0, 1
+
+SLIDING_GEOM_BF16 = dict(head_dim=256, theta=1e4, rotary_fraction=1.0, window=512)
+FULL_GEOM_BF16 = dict(head_dim=512, theta=1e6, rotary_fraction=0.25, window=0)
+
+CONFIGS = {
+    "tiny_fp32_stack": dict(
+        B=1, T=64, H=4, Hkv=2, dtype=F32, seed=0,
+        types=[SLIDING, FULL, SLIDING, FULL], n_shared=2,
+        geom={SLIDING: dict(head_dim=64, theta=1e4, rotary_fraction=1.0, window=16),
+              FULL: dict(head_dim=128, theta=1e6, rotary_fraction=0.25, window=0)}),
+    "prefill_bf16": dict(
+        B=1, T=2048, H=8, Hkv=2, dtype=BF16, seed=1,
+        types=[SLIDING, FULL], n_shared=0,
+        geom={SLIDING: SLIDING_GEOM_BF16, FULL: FULL_GEOM_BF16}),
+    "decode_bf16": dict(
+        B=64, L_lo=1024, L_hi=8192, H=8, Hkv=2, dtype=BF16, seed=2,
+        types=[SLIDING, FULL], n_shared=0,
+        geom={SLIDING: SLIDING_GEOM_BF16, FULL: FULL_GEOM_BF16}),
+    "stack42_bf16": dict(
+        B=8, T=4096, decode_steps=128, H=8, Hkv=2, dtype=BF16, seed=3,
+        types=[FULL if (i + 1) % 6 == 0 else SLIDING for i in range(42)], n_shared=18,
+        geom={SLIDING: SLIDING_GEOM_BF16, FULL: FULL_GEOM_BF16}),
+    "longctx_decode_bf16": dict(
+        B=4, L=131072, H=8, Hkv=2, dtype=BF16, seed=4,
+        types=[FULL, SLIDING], n_shared=0,
+        geom={SLIDING: SLIDING_GEOM_BF16, FULL: FULL_GEOM_BF16}),
+}
+
+EPS = 1e-6
+ATTN_SCALE = 1.0
+
+
+def torch_dtype(dtype):
+    return torch.bfloat16 if dtype == BF16 else torch.float32
+
+
+def layer_geometry(cfg, layer):
+    """Per-layer hyperparameters of a workload (type, head width, theta, ...)."""
+    lt = cfg["types"][layer]
+    g = cfg["geom"][lt]
+    return dict(layer_type=lt, head_dim=g["head_dim"], n_heads=cfg["H"], n_kv_heads=cfg["Hkv"],
+                window=g["window"], theta=g["theta"], rotary_fraction=g["rotary_fraction"],
+                eps=EPS, attn_scale=ATTN_SCALE, dtype=cfg["dtype"])
+
+
+def seed_for(base, layer, tensor, step=0):
+    """Distinct, reproducible seed per (workload, layer, tensor, decode step)."""
+    return ((base * 1_000_003 + layer) * 131 + tensor) * 10_007 + step
+
+
+def normal(shape, seed, dtype, device="cpu"):
+    """N(0,1) draws from a seeded torch generator on ``device``, cast to dtype."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    x = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    return x.to(torch_dtype(dtype)) if dtype in (F32, BF16) else x.to(dtype)
+
+
+def norm_weight(head_dim, seed):
+    """Norm weight 1 + 0.1 N(0,1), float32, on the CPU."""
+    g = torch.Generator()
+    g.manual_seed(seed)
+    return 1.0 + 0.1 * torch.randn(head_dim, generator=g, dtype=torch.float32)
+
+
+def lengths(B, lo, hi, seed):
+    """KV lengths uniform over the integers [lo, hi]."""
+    g = torch.Generator()
+    g.manual_seed(seed)
+    return torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int32)
+
+
+def layer_inputs(cfg, layer, T, owns_cache, device="cpu", step=0, B=None):
+    """Raw q/k/v of one layer for T tokens, and its norm weights.
+
+    Returns dict(q [B,T,H,hd], k / v [B,T,Hkv,hd] (absent on a shared layer),
+    q_norm_w [hd] f32, k_norm_w [hd] f32 (absent on a shared layer)).
+    """
+    geo = layer_geometry(cfg, layer)
+    hd, H, Hkv, dt = geo["head_dim"], cfg["H"], cfg["Hkv"], cfg["dtype"]
+    B = cfg["B"] if B is None else B
+    s = cfg["seed"]
+    out = dict(q=normal((B, T, H, hd), seed_for(s, layer, 0, step), dt, device),
+               q_norm_w=norm_weight(hd, seed_for(s, layer, 3)))
+    if owns_cache:
+        out["k"] = normal((B, T, Hkv, hd), seed_for(s, layer, 1, step), dt, device)
+        out["v"] = normal((B, T, Hkv, hd), seed_for(s, layer, 2, step), dt, device)
+        out["k_norm_w"] = norm_weight(hd, seed_for(s, layer, 4))
+    return out
+
+
+def prefilled_cache(cfg, layer, Lmax, device="cpu", B=None):
+    """A KV cache whose rows already hold N(0,1) values (decode workloads)."""
+    geo = layer_geometry(cfg, layer)
+    hd, Hkv, dt = geo["head_dim"], cfg["Hkv"], cfg["dtype"]
+    B = cfg["B"] if B is None else B
+    s = cfg["seed"]
+    k = normal((B, Hkv, Lmax, hd), seed_for(s, layer, 5), dt, device)
+    v = normal((B, Hkv, Lmax, hd), seed_for(s, layer, 6), dt, device)
+    return k, v
