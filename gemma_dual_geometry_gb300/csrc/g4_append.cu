@@ -1,0 +1,142 @@
+// Step a4: fused per-head RMSNorm -> rotate_half RoPE -> KV-cache append.
+//
+// cortiq-engine g4e.rs `g4e_forward` (attention block): q heads are normed
+// with q_norm and roped; on a layer that owns its cache, k heads are normed
+// with k_norm and roped, v heads get the weight-less norm (`rms_plain`), and
+// both are appended at the token's position.  ferrox-models
+// gemma4_engine.rs `forward_token_on_worker` does the same per head
+// (`rms_norm_per_head`, `apply_rope`, `cache.push`).  turbospark-runtime
+// gemma4/attn.rs writes the projections straight into the cache slot and
+// norms/ropes them there, which is the fusion done here.
+//
+// One CTA (4 warps) per token handles rows_per_cta of its H + 2*Hkv head
+// rows; one warp per head row.  The token's cos/sin table (head_dim / 2
+// pairs) is built once per CTA: angle = pos * inv_freq[j] with inv_freq a
+// float32 table, reduced modulo 2*pi in float64 (exact product, one fma), then
+// sincosf of the reduced float angle.  Pairs j >= n_rot (zero inv_freq) are
+// left untouched, so those dims are the normed input bit for bit.
+//
+// Lane l of a warp owns elements [l*E, l*E + E) of the lower half and the
+// same offsets of the upper half (E = head_dim / 64), so each rotate_half
+// pair (j, j + head_dim/2) sits in one lane.
+#include "g4_device.cuh"
+#include "g4_internal.h"
+
+namespace g4 {
+namespace {
+
+constexpr double kInv2Pi = 0.15915494309189533576888376337251;  // 1 / (2 pi)
+constexpr double k2Pi = 6.2831853071795864769252867665590;      // 2 pi
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(128) append_normrope_kernel(const __grid_constant__ AppendArgs a) {
+  constexpr int HALF = HD / 2;
+  constexpr int E = HD / 64;
+  __shared__ float s_cos[HALF];
+  __shared__ float s_sin[HALF];
+
+  const int tok = blockIdx.x;  // b * T + t
+  const int b = tok / a.T;
+  const int pos = a.positions[tok];
+
+  for (int j = threadIdx.x; j < HALF; j += blockDim.x) {
+    float c = 1.0f, s = 0.0f;
+    if (j < a.n_rot) {
+      const double ang = static_cast<double>(pos) * static_cast<double>(a.inv_freq[j]);
+      const double k = rint(ang * kInv2Pi);
+      const double r = fma(-k, k2Pi, ang);
+      sincosf(static_cast<float>(r), &s, &c);
+    }
+    s_cos[j] = c;
+    s_sin[j] = s;
+  }
+  __syncthreads();
+
+  const bool owns = a.k_in != nullptr;
+  const int nrows = a.H + (owns ? 2 * a.Hkv : 0);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int row0 = blockIdx.y * a.rows_per_cta;
+  const int row1 = min(nrows, row0 + a.rows_per_cta);
+  const bool pos_ok = pos >= 0 && pos < a.max_len;
+
+  for (int row = row0 + warp; row < row1; row += 4) {
+    const T* src;
+    T* dst;
+    const float* w;
+    bool rope;
+    if (row < a.H) {  // q head
+      const size_t off = (static_cast<size_t>(tok) * a.H + row) * HD;
+      src = static_cast<const T*>(a.q_in) + off;
+      dst = static_cast<T*>(a.q_out) + off;
+      w = a.q_w;
+      rope = true;
+    } else {
+      const bool is_k = row < a.H + a.Hkv;
+      const int kvh = is_k ? row - a.H : row - a.H - a.Hkv;
+      if (!pos_ok) continue;
+      src = static_cast<const T*>(is_k ? a.k_in : a.v_in) + (static_cast<size_t>(tok) * a.Hkv + kvh) * HD;
+      dst = static_cast<T*>(is_k ? a.cache_k : a.cache_v) +
+            ((static_cast<size_t>(b) * a.Hkv + kvh) * a.max_len + pos) * HD;
+      w = is_k ? a.k_w : nullptr;
+      rope = is_k;
+    }
+    float x[2 * E];
+    load_elems<E>(src + lane * E, x);
+    load_elems<E>(src + HALF + lane * E, x + E);
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 2 * E; ++i) ss = fmaf(x[i], x[i], ss);
+    ss = warp_sum(ss);
+    const float inv = 1.0f / sqrtf(ss / static_cast<float>(HD) + a.eps);
+    if (w != nullptr) {
+      float wl[E], wh[E];
+      load_elems<E>(w + lane * E, wl);
+      load_elems<E>(w + HALF + lane * E, wh);
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        x[i] = x[i] * inv * wl[i];
+        x[E + i] = x[E + i] * inv * wh[i];
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 2 * E; ++i) x[i] *= inv;
+    }
+    if (rope) {
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        const int j = lane * E + i;
+        if (j < a.n_rot) {
+          const float c = s_cos[j], s = s_sin[j];
+          const float lo = x[i], hi = x[E + i];
+          x[i] = lo * c - hi * s;
+          x[E + i] = hi * c + lo * s;
+        }
+      }
+    }
+    store_elems<E>(dst + lane * E, x);
+    store_elems<E>(dst + HALF + lane * E, x + E);
+  }
+}
+
+template <typename T>
+cudaError_t launch_t(const AppendArgs& a, cudaStream_t s) {
+  const int nrows = a.H + (a.k_in ? 2 * a.Hkv : 0);
+  dim3 grid(a.B * a.T, (nrows + a.rows_per_cta - 1) / a.rows_per_cta);
+  switch (a.hd) {
+    case 64: append_normrope_kernel<T, 64><<<grid, 128, 0, s>>>(a); break;
+    case 128: append_normrope_kernel<T, 128><<<grid, 128, 0, s>>>(a); break;
+    case 256: append_normrope_kernel<T, 256><<<grid, 128, 0, s>>>(a); break;
+    case 512: append_normrope_kernel<T, 512><<<grid, 128, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs& a, int dtype, cudaStream_t s) {
+  return dtype == 1 ? launch_t<__nv_bfloat16>(a, s) : launch_t<float>(a, s);
+}
+
+}  // namespace g4

@@ -1,0 +1,439 @@
+// Steps a6 (decode) and a5 in float32: causal GQA softmax attention on CUDA
+// cores, split over the key range (split-KV), HBM-bound.
+//
+// Semantics (cortiq-engine g4e.rs `attend_all_heads(q, caches[src], ..., 1.0,
+// window, ...)`; ferrox-models gemma4_engine.rs `causal_gqa_attention[_windowed]`;
+// turbospark-runtime gemma4/attn.rs `kv_start = seq_len - sliding_window`):
+// query head h reads kv head h / G (G = H / Hkv, contiguous groups as in
+// taconite `text_attention`), keys [kstart, L) with kstart = L - window on
+// sliding layers and 0 on full layers, scores scaled by attn_scale (1.0).
+//
+// Work decomposition: one CTA per (split, kv head, query row).  All G query
+// heads of the kv head share every K/V row the CTA streams, so each key row
+// is read from HBM once per query row.  Each of the 4 warps owns a ring of
+// 3 shared-memory stages filled by non-tensor bulk copies
+// (cp.async.bulk, one K and one V copy per stage, completing on the stage's
+// mbarrier); stages of the CTA's key range go to the warps round-robin.
+//
+// Inside a warp, lane l owns HD/32 elements of every row (16-byte pieces
+// l, l+32, ... so shared-memory reads are conflict-free).  For a batch of
+// KB = 16/G keys the lane forms KB*G partial dot products with packed f32x2
+// FMAs, a butterfly reduce-scatter turns the 16 partials of 32 lanes into
+// 16 full scores, the scores go through shared memory so every lane holds
+// all of them, and the online softmax (log2 domain; q is pre-scaled by
+// attn_scale*log2(e)) and the P.V update run redundantly per lane with no
+// further shuffles.  Warps merge their (m, l, o) at the end; with one split
+// the CTA writes the normalised output, otherwise an un-normalised partial
+// that launch_attn_combine merges with log-sum-exp weights.
+#include <math.h>
+
+#include "g4_device.cuh"
+#include "g4_internal.h"
+
+namespace g4 {
+namespace {
+
+constexpr int kNW = 4;   // warps per CTA
+constexpr int kNST = 3;  // stages per warp
+constexpr int kNP = 16;  // partial scores per reduce-scatter batch
+
+// Sum of v[i] over the 32 lanes, scattered: lane l returns the total of index l >> 1.
+__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int n = 16, o = 16; n > 1; n >>= 1, o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = up ? v[i] : v[i + n / 2];
+      const float keep = up ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
+template <typename T, int HD, int G>
+struct SimtCfg {
+  static constexpr int ES = sizeof(T);
+  static constexpr int EL = HD / 32;                 // elements per lane per row
+  static constexpr int CHE = 16 / ES;                // elements per 16-byte piece
+  static constexpr int PE = EL < CHE ? EL : CHE;     // elements per piece a lane reads
+  static constexpr int NPC = EL / PE;                // pieces per lane per row
+  static constexpr int KB = kNP / G;                 // keys per reduce batch
+  static constexpr int ROWB = HD * ES;               // bytes per cache row
+  static constexpr int NB = (KB * ROWB >= 2048) ? 1 : 2048 / (KB * ROWB);  // batches per stage
+  static constexpr int SK = KB * NB;                 // keys per stage
+  static constexpr int STAGE_B = SK * ROWB;          // bytes of K (and of V) per stage
+  static constexpr int RING_B = kNW * kNST * 2 * STAGE_B;
+  static constexpr int MERGE_B = kNW * G * (HD + 2) * 4;
+  static constexpr int AREA_B = RING_B > MERGE_B ? RING_B : MERGE_B;
+  static constexpr int SMEM_B = AREA_B + kNW * kNST * 8 + kNW * kNP * 4;
+};
+
+template <typename T, int NPC, int PE>
+__device__ __forceinline__ void load_row_f2(const T* row, int lane, float2 (&x)[NPC * PE / 2]) {
+  float f[NPC * PE];
+#pragma unroll
+  for (int c = 0; c < NPC; ++c) load_elems<PE>(row + (lane + 32 * c) * PE, f + c * PE);
+#pragma unroll
+  for (int i = 0; i < NPC * PE / 2; ++i) x[i] = make_float2(f[2 * i], f[2 * i + 1]);
+}
+
+template <typename T, int HD, int G>
+__global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_constant__ AttnSimtArgs a) {
+  using C = SimtCfg<T, HD, G>;
+  constexpr int EL2 = C::EL / 2;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::AREA_B);
+  float* sc_all = reinterpret_cast<float*>(bars + kNW * kNST);
+
+  const int split = blockIdx.x % a.nsplit;
+  const int rest = blockIdx.x / a.nsplit;
+  const int kvh = rest % a.Hkv;
+  const int bt = rest / a.Hkv;  // b * T + t
+  const int b = bt / a.T;
+  const int t = bt % a.T;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Query position and visible key range [kbeg, L).
+  int L;
+  if (a.mode == 0) {
+    L = min(max(a.base[b], 1), a.len_cap);
+  } else {
+    L = min(max(a.base[b] + t, 0), a.max_len - 1) + 1;
+  }
+  const int kbeg = a.sliding ? max(0, L - a.window) : 0;
+  const int k0 = kbeg + split * a.chunk;
+  const int k1 = min(L, k0 + a.chunk);
+  const int nkeys = max(0, k1 - k0);
+  const int nstages = (nkeys + C::SK - 1) / C::SK;
+
+  uint8_t* ring = smem + warp * (kNST * 2 * C::STAGE_B);
+  uint64_t* wbar = bars + warp * kNST;
+  float* sc = sc_all + warp * kNP;
+  bool aborted = false;
+
+  if (lane == 0) {
+    for (int i = 0; i < kNST; ++i) mbar_init(smem_u32(&wbar[i]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const size_t head_base = (static_cast<size_t>(b) * a.Hkv + kvh) * a.max_len;
+  const T* gk = static_cast<const T*>(a.ck) + head_base * HD;
+  const T* gv = static_cast<const T*>(a.cv) + head_base * HD;
+
+  auto issue = [&](int st_idx, int buf) {
+    const int kk0 = k0 + st_idx * C::SK;
+    const int n = min(C::SK, k1 - kk0);
+    const uint32_t bytes = static_cast<uint32_t>(n) * C::ROWB;
+    const uint32_t bar = smem_u32(&wbar[buf]);
+    mbar_arrive_expect_tx(bar, 2 * bytes);
+    bulk_g2s(smem_u32(ring + buf * 2 * C::STAGE_B), gk + static_cast<size_t>(kk0) * HD, bytes, bar);
+    bulk_g2s(smem_u32(ring + buf * 2 * C::STAGE_B + C::STAGE_B), gv + static_cast<size_t>(kk0) * HD, bytes, bar);
+  };
+
+  if (lane == 0) {
+    for (int i = 0; i < kNST; ++i) {
+      const int st = warp + i * kNW;
+      if (st < nstages) issue(st, i);
+    }
+  }
+
+  // q of the G heads, pre-scaled into the log2 domain.
+  float2 q2[G][EL2];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const T* qrow = static_cast<const T*>(a.q) + (static_cast<size_t>(bt) * a.H + kvh * G + h) * HD;
+    load_row_f2<T, C::NPC, C::PE>(qrow, lane, q2[h]);
+#pragma unroll
+    for (int i = 0; i < EL2; ++i) {
+      q2[h][i].x *= a.scale_log2;
+      q2[h][i].y *= a.scale_log2;
+    }
+  }
+
+  float m[G], l[G];
+  float2 o2[G][EL2];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < EL2; ++i) o2[h][i] = make_float2(0.0f, 0.0f);
+  }
+
+  int consumed = 0;  // stages this warp has finished (for draining after an abort)
+  for (int it = 0;; ++it) {
+    const int st_idx = warp + it * kNW;
+    if (st_idx >= nstages) break;
+    const int buf = it % kNST;
+    if (!warp_wait(smem_u32(&wbar[buf]), (it / kNST) & 1, a.err)) {
+      aborted = true;
+      break;
+    }
+    const int n = min(C::SK, k1 - (k0 + st_idx * C::SK));
+    const T* sk = reinterpret_cast<const T*>(ring + buf * 2 * C::STAGE_B);
+    const T* sv = reinterpret_cast<const T*>(ring + buf * 2 * C::STAGE_B + C::STAGE_B);
+
+#pragma unroll 1
+    for (int nb = 0; nb < C::NB; ++nb) {
+      const int kb0 = nb * C::KB;
+      if (kb0 >= n) break;
+      // Partial dot products: part[key * G + h].
+      float part[kNP];
+#pragma unroll
+      for (int key = 0; key < C::KB; ++key) {
+        float2 kx[EL2];
+        load_row_f2<T, C::NPC, C::PE>(sk + (kb0 + key) * HD, lane, kx);
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+          for (int i = 0; i < EL2; ++i) acc = __ffma2_rn(q2[h][i], kx[i], acc);
+          part[key * G + h] = acc.x + acc.y;
+        }
+      }
+      const float s = reduce_scatter16(part, lane);
+      if ((lane & 1) == 0) sc[lane >> 1] = s;
+      __syncwarp();
+      float sv_all[kNP];
+#pragma unroll
+      for (int i = 0; i < kNP / 4; ++i) {
+        const float4 v4 = reinterpret_cast<const float4*>(sc)[i];
+        sv_all[4 * i] = v4.x; sv_all[4 * i + 1] = v4.y; sv_all[4 * i + 2] = v4.z; sv_all[4 * i + 3] = v4.w;
+      }
+      __syncwarp();
+      float p[C::KB][G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float mb = -INFINITY;
+#pragma unroll
+        for (int key = 0; key < C::KB; ++key)
+          if (kb0 + key < n) mb = fmaxf(mb, sv_all[key * G + h]);
+        const float m_new = fmaxf(m[h], mb);
+        const float alpha = (m[h] == -INFINITY) ? 0.0f : exp2f(m[h] - m_new);
+        float ps = 0.0f;
+#pragma unroll
+        for (int key = 0; key < C::KB; ++key) {
+          p[key][h] = (kb0 + key < n) ? exp2f(sv_all[key * G + h] - m_new) : 0.0f;
+          ps += p[key][h];
+        }
+        l[h] = l[h] * alpha + ps;
+        m[h] = m_new;
+        if (alpha != 1.0f) {
+#pragma unroll
+          for (int i = 0; i < EL2; ++i) {
+            o2[h][i].x *= alpha;
+            o2[h][i].y *= alpha;
+          }
+        }
+      }
+      // o += p . v
+#pragma unroll
+      for (int key = 0; key < C::KB; ++key) {
+        if (kb0 + key < n) {
+          float2 vx[EL2];
+          load_row_f2<T, C::NPC, C::PE>(sv + (kb0 + key) * HD, lane, vx);
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+            const float2 pp = make_float2(p[key][h], p[key][h]);
+#pragma unroll
+            for (int i = 0; i < EL2; ++i) o2[h][i] = __ffma2_rn(pp, vx[i], o2[h][i]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    consumed = it + 1;
+    const int next = st_idx + kNST * kNW;
+    if (lane == 0 && next < nstages) issue(next, buf);
+  }
+
+  // After an abort, wait (bounded) for copies this warp still has in flight.
+  if (aborted) {
+    for (int it = consumed;; ++it) {
+      const int st_idx = warp + it * kNW;
+      if (st_idx >= nstages || it >= consumed + kNST) break;
+      warp_wait(smem_u32(&wbar[it % kNST]), (it / kNST) & 1, nullptr);
+    }
+  }
+  __syncthreads();
+
+  // Merge the warps' (m, l, o) through shared memory (the ring is free now).
+  float* ms = reinterpret_cast<float*>(smem);          // [NW][G]
+  float* ls = ms + kNW * G;                            // [NW][G]
+  float* os = ls + kNW * G;                            // [NW][G][HD]
+  if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      ms[warp * G + h] = m[h];
+      ls[warp * G + h] = l[h];
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float* orow = os + (warp * G + h) * HD;
+#pragma unroll
+    for (int c = 0; c < C::NPC; ++c) {
+      float f[C::PE];
+#pragma unroll
+      for (int e = 0; e < C::PE; e += 2) {
+        f[e] = o2[h][(c * C::PE + e) / 2].x;
+        f[e + 1] = o2[h][(c * C::PE + e) / 2].y;
+      }
+      store_elems<C::PE>(orow + (lane + 32 * c) * C::PE, f);
+    }
+  }
+  __syncthreads();
+
+  for (int idx = threadIdx.x; idx < G * HD; idx += blockDim.x) {
+    const int h = idx / HD;
+    const int d = idx % HD;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kNW; ++w) M = fmaxf(M, ms[w * G + h]);
+    float O = 0.0f, Ls = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kNW; ++w) {
+        const float mw = ms[w * G + h];
+        if (mw != -INFINITY) {
+          const float f = exp2f(mw - M);
+          O += f * os[(w * G + h) * HD + d];
+          Ls += f * ls[w * G + h];
+        }
+      }
+    }
+    const int head = kvh * G + h;
+    if (a.nsplit == 1) {
+      const float val = (Ls > 0.0f) ? O / Ls : 0.0f;
+      T* dst = static_cast<T*>(a.out) + (static_cast<size_t>(bt) * a.H + head) * HD + d;
+      store_elems<1>(dst, &val);
+    } else {
+      const size_t pidx = (static_cast<size_t>(bt) * a.H + head) * a.nsplit + split;
+      a.ws_o[pidx * HD + d] = O;
+      if (d == 0) {
+        a.ws_m[pidx] = M;
+        a.ws_l[pidx] = Ls;
+      }
+    }
+  }
+}
+
+// Log-sum-exp merge of the split partials of one (query row, head).
+template <typename T, int HD>
+__global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnSimtArgs a) {
+  const int head = blockIdx.x;
+  const int bt = blockIdx.y;
+  const size_t p0 = (static_cast<size_t>(bt) * a.H + head) * a.nsplit;
+  float M = -INFINITY;
+  for (int s = 0; s < a.nsplit; ++s) M = fmaxf(M, a.ws_m[p0 + s]);
+  float Ls = 0.0f;
+  for (int s = 0; s < a.nsplit; ++s) {
+    const float ms = a.ws_m[p0 + s];
+    if (ms != -INFINITY) Ls += exp2f(ms - M) * a.ws_l[p0 + s];
+  }
+  const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+  T* dst = static_cast<T*>(a.out) + (static_cast<size_t>(bt) * a.H + head) * HD;
+  for (int d = threadIdx.x; d < HD; d += blockDim.x) {
+    float O = 0.0f;
+    for (int s = 0; s < a.nsplit; ++s) {
+      const float ms = a.ws_m[p0 + s];
+      if (ms != -INFINITY) O += exp2f(ms - M) * a.ws_o[(p0 + s) * HD + d];
+    }
+    const float val = O * inv;
+    store_elems<1>(dst + d, &val);
+  }
+}
+
+template <typename T, int HD, int G>
+cudaError_t launch_simt_hg(const AttnSimtArgs& a, cudaStream_t s) {
+  using C = SimtCfg<T, HD, G>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::SMEM_B);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const long long nblk = static_cast<long long>(a.nsplit) * a.Hkv * a.B * a.T;
+  attn_simt_kernel<T, HD, G><<<static_cast<unsigned>(nblk), kNW * 32, C::SMEM_B, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T, int HD>
+cudaError_t launch_simt_h(const AttnSimtArgs& a, cudaStream_t s) {
+  const int G = a.H / a.Hkv;
+  switch (G) {
+    case 1: return launch_simt_hg<T, HD, 1>(a, s);
+    case 2: return launch_simt_hg<T, HD, 2>(a, s);
+    case 4: return launch_simt_hg<T, HD, 4>(a, s);
+    case 8:
+      if constexpr (HD <= 256) return launch_simt_hg<T, HD, 8>(a, s);
+      return cudaErrorInvalidValue;
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename T>
+cudaError_t launch_simt_t(const AttnSimtArgs& a, cudaStream_t s) {
+  switch (a.hd) {
+    case 64: return launch_simt_h<T, 64>(a, s);
+    case 128: return launch_simt_h<T, 128>(a, s);
+    case 256: return launch_simt_h<T, 256>(a, s);
+    case 512: return launch_simt_h<T, 512>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <typename T>
+cudaError_t launch_combine_t(const AttnSimtArgs& a, cudaStream_t s) {
+  dim3 grid(a.H, a.B * a.T);
+  switch (a.hd) {
+    case 64: attn_combine_kernel<T, 64><<<grid, 128, 0, s>>>(a); break;
+    case 128: attn_combine_kernel<T, 128><<<grid, 128, 0, s>>>(a); break;
+    case 256: attn_combine_kernel<T, 256><<<grid, 128, 0, s>>>(a); break;
+    case 512: attn_combine_kernel<T, 512><<<grid, 128, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_simt(const AttnSimtArgs& a, int dtype, cudaStream_t s) {
+  return dtype == 1 ? launch_simt_t<__nv_bfloat16>(a, s) : launch_simt_t<float>(a, s);
+}
+
+cudaError_t launch_attn_combine(const AttnSimtArgs& a, int dtype, cudaStream_t s) {
+  return dtype == 1 ? launch_combine_t<__nv_bfloat16>(a, s) : launch_combine_t<float>(a, s);
+}
+
+DecodePlan decode_plan(int sliding, int window, int hd, int H, int Hkv, int B, int max_seq_len) {
+  DecodePlan p;
+  const int span = sliding ? (max_seq_len < window ? max_seq_len : window) : max_seq_len;
+  const int units = B * Hkv;
+  const int target_ctas = 1216;  // eight CTAs per SM on a 152-SM GPU
+  int nsplit = (target_ctas + units - 1) / units;
+  const int by_len = (span + 255) / 256;  // at least 256 keys per split
+  if (nsplit > by_len) nsplit = by_len;
+  if (nsplit < 1) nsplit = 1;
+  int chunk = (span + nsplit - 1) / nsplit;
+  chunk = (chunk + 63) / 64 * 64;
+  nsplit = (span + chunk - 1) / chunk;
+  p.chunk = chunk;
+  p.nsplit = nsplit;
+  if (nsplit <= 1) {
+    p.ws_bytes = 0;
+  } else {
+    const size_t np = static_cast<size_t>(B) * H * nsplit;
+    const size_t o_b = (np * hd * 4 + 255) / 256 * 256;
+    const size_t m_b = (np * 4 + 255) / 256 * 256;
+    p.ws_bytes = o_b + 2 * m_b;
+  }
+  return p;
+}
+
+}  // namespace g4

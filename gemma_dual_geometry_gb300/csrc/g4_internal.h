@@ -1,0 +1,78 @@
+// Internal launch interface between the C-ABI front end (g4_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace g4 {
+
+constexpr int kMaxHalf = 256;  // head_dim / 2 for the widest supported head (512)
+
+// Step a4: norm -> RoPE -> cache append.
+struct AppendArgs {
+  const void* q_in;
+  const void* k_in;  // null on a shared layer
+  const void* v_in;
+  const float* q_w;
+  const float* k_w;
+  const int32_t* positions;  // [B*T]
+  void* q_out;
+  void* cache_k;  // [B][Hkv][max_len][hd]
+  void* cache_v;
+  int B, T, H, Hkv, hd, max_len;
+  int rows_per_cta;  // head rows (of H + 2 Hkv) handled per CTA
+  int n_rot;         // rotated pairs; inv_freq[j] == 0 for j >= n_rot
+  float eps;
+  float inv_freq[kMaxHalf];
+};
+cudaError_t launch_append(const AppendArgs& a, int dtype, cudaStream_t s);
+
+// Steps a5 (float32) and a6: split-KV softmax attention on CUDA cores.
+// mode 0 (decode): one query per sequence at position base[b] - 1, keys
+//   [kstart, base[b]); mode 1 (prefill): query t at position base[b] + t.
+struct AttnSimtArgs {
+  const void* q;    // [B][T][H][hd]
+  const void* ck;   // [B][Hkv][max_len][hd]
+  const void* cv;
+  void* out;        // [B][T][H][hd]
+  const int32_t* base;
+  float* ws_o;      // [B*T][H][nsplit][hd] partial outputs (nsplit > 1)
+  float* ws_m;      // [B*T][H][nsplit] running max (log2 domain)
+  float* ws_l;      // [B*T][H][nsplit] softmax denominators
+  int* err;
+  int mode;
+  int B, T, H, Hkv, hd, max_len;
+  int sliding, window;
+  int len_cap;      // decode: lengths clamped to [1, len_cap]
+  int chunk;        // keys per split
+  int nsplit;
+  float scale_log2;  // attn_scale * log2(e)
+};
+cudaError_t launch_attn_simt(const AttnSimtArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_attn_combine(const AttnSimtArgs& a, int dtype, cudaStream_t s);
+
+// Step a5 (bf16): tcgen05 flash prefill.
+struct PrefillTcArgs {
+  const void* q;     // [B][T][H][hd] bf16
+  const void* ck;    // [B][Hkv][max_len][hd] bf16
+  const void* cv;
+  void* out;         // [B][T][H][hd] bf16
+  const int32_t* q_start;  // [B]
+  int* err;
+  int B, T, H, Hkv, hd, max_len;
+  int sliding, window;
+  float scale_log2;
+};
+cudaError_t launch_prefill_tc(const PrefillTcArgs& a, cudaStream_t s);
+
+// Decode split plan shared by the workspace query and the launch.
+struct DecodePlan {
+  int chunk;
+  int nsplit;
+  size_t ws_bytes;
+};
+DecodePlan decode_plan(int sliding, int window, int hd, int H, int Hkv, int B, int max_seq_len);
+
+}  // namespace g4

@@ -1,0 +1,213 @@
+/*
+ * g4attn.h -- C ABI of the GB300 (sm_103a) Gemma-4 E-series dual-geometry
+ * attention path.
+ *
+ * The path, per layer of an attention-only stack:
+ *   1. g4_kv_append_normrope: per-head RMSNorm of q and k (plain x-hat * w,
+ *      eps inside the mean), weight-less RMSNorm of v, rotate_half RoPE on q
+ *      and k, and the write of k and v into the layer's KV cache.
+ *   2. g4_attn_prefill / g4_attn_decode: causal GQA softmax attention with
+ *      score scale attn_scale (1.0 for Gemma-4), windowed on sliding layers,
+ *      over the cache of the layer itself or, on a shared-KV tail layer, of
+ *      its source layer.
+ *
+ * Sources (page title + item):
+ *   cortiq-engine g4e.rs: `rms`, `rms_plain`, `G4eGlobals` (inv_freq tables,
+ *     window "current included"), `G4eLayer` (kv_share_src, sliding, hd),
+ *     `g4e_forward` attention block.
+ *   ferrox-models gemma4_engine.rs: `Gemma4Hparams` (head_dim per type,
+ *     has_kv, kv_reuse_layer, rope_theta_for, attention_scale = 1.0),
+ *     `forward_token_on_worker` (norm per head, RoPE, push, windowed /
+ *     unwindowed causal GQA attention, shared-KV head_dim check).
+ *   taconite-embeddinggemma2 model.rs: `rope_half`, `text_attention`
+ *     (rotate_half pairing, head grouping kh = hh / group).
+ *   turbospark-runtime gemma4/attn.rs: `encode_gemma4_layer_attn_and_router`
+ *     (RMS_EPS = 1e-6, rotated_pairs, kv_start = seq_len - sliding_window).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers owned by the caller; the
+ *     library allocates no device memory and keeps no state between calls
+ *     except a thread-local error message and one device-side error word
+ *     (see g4_take_device_error).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream).  A call that returns G4_OK has only
+ *     enqueued work.
+ *   - Host-detectable errors return a status before anything is launched;
+ *     nothing is written then.  g4_last_error() gives the message.
+ *   - Device-side values (positions, lengths) cannot be checked on the host.
+ *     Kernels clamp them so that no access leaves the buffers; rows with
+ *     out-of-contract values get unspecified contents.
+ *   - Pointers to q/k/v/out/cache must be 16-byte aligned.
+ *   - dtype is per layer and covers q_in/k_in/v_in, the cache, q_out and the
+ *     attention output alike: G4_F32 (float) or G4_BF16 (bfloat16, RNE on
+ *     every store).  Norm weights are always float32.  Arithmetic is float32
+ *     with float32 accumulation (bf16 tensor-core inputs in bf16 prefill).
+ */
+#ifndef G4ATTN_H
+#define G4ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  G4_OK = 0,
+  G4_ERR_INVALID_ARG = 1,    /* null / misaligned pointer, bad size or field      */
+  G4_ERR_UNSUPPORTED = 2,    /* head_dim or GQA group not built                    */
+  G4_ERR_SHARE_MISMATCH = 3, /* shared layer's source cache has another type,
+                                head_dim, kv-head count or dtype                   */
+  G4_ERR_CAPACITY = 4,       /* batch or length larger than the cache              */
+  G4_ERR_WORKSPACE = 5,      /* decode workspace too small                         */
+  G4_ERR_CUDA = 6            /* a CUDA runtime/driver call or launch failed        */
+} g4_status;
+
+typedef enum { G4_SLIDING = 0, G4_FULL = 1 } g4_layer_type;
+typedef enum { G4_F32 = 0, G4_BF16 = 1 } g4_dtype;
+
+/*
+ * Per-layer attention hyperparameters (ferrox-models `Gemma4Hparams`,
+ * cortiq-engine `G4eLayer`).
+ *   layer_type      G4_SLIDING or G4_FULL.
+ *   head_dim        this layer's head width: head_dim on sliding layers,
+ *                   global_head_dim on full layers.  64, 128, 256 or 512.
+ *   n_heads         query heads H; n_kv_heads Hkv divides it and the group
+ *                   H / Hkv is 1, 2, 4 or 8 (with group * head_dim <= 2048).
+ *   window          sliding window in tokens, current token included (a key
+ *                   j is visible from query i iff j <= i and i - j < window).
+ *                   Must be >= 1 on sliding layers; ignored on full layers.
+ *   theta           RoPE base (local theta on sliding, model theta on full).
+ *   rotary_fraction fraction of the head that is rotated: the first
+ *                   floor(head_dim * rotary_fraction / 2) pairs rotate with
+ *                   inv_freq[j] = theta^(-2j / head_dim); the other pairs have
+ *                   inv_freq 0 (identity).  1.0 on sliding layers, the
+ *                   partial-rotary factor (e.g. 0.25) on full layers.
+ *   eps             RMSNorm epsilon (1e-6), added to the mean square.
+ *   attn_scale      score scale, > 0 (Gemma-4: 1.0).
+ *   kv_share_src    -1 if the layer owns its cache, else the index of the
+ *                   layer whose cache it reads (see g4_kv_share_src).
+ *   dtype           g4_dtype of every tensor of the layer.
+ */
+typedef struct {
+  int32_t layer_type;
+  int32_t head_dim;
+  int32_t n_heads;
+  int32_t n_kv_heads;
+  int32_t window;
+  float theta;
+  float rotary_fraction;
+  float eps;
+  float attn_scale;
+  int32_t kv_share_src;
+  int32_t dtype;
+} g4_layer_params;
+
+/*
+ * One layer's KV cache, caller-owned device memory, layout
+ * k[batch][n_kv_heads][max_len][head_dim] (same for v): rows of head_dim
+ * contiguous, one row per token position.  Layers that read another layer's
+ * cache may leave their entry zeroed.
+ */
+typedef struct {
+  void* k;
+  void* v;
+  int32_t layer_type;
+  int32_t head_dim;
+  int32_t n_kv_heads;
+  int32_t max_len;
+  int32_t batch;
+  int32_t dtype;
+} g4_kv_cache;
+
+/*
+ * Shared-KV routing (ferrox-models `Gemma4Hparams::kv_reuse_layer`;
+ * cortiq-engine g4e.rs module doc).  With first_shared = n_layers - n_shared:
+ * returns -1 for layer < first_shared (owns its cache), first_shared - 2 for a
+ * sliding tail layer and first_shared - 1 for a full tail layer.
+ * is_sliding[n_layers] holds 1 for sliding layers.  Returns -2 on invalid
+ * arguments (n_layers < 1, n_shared outside [0, n_layers), layer out of range,
+ * NULL is_sliding, or a source index < 0).  Host only.
+ */
+int32_t g4_kv_share_src(int32_t n_layers, int32_t n_shared, const int32_t* is_sliding, int32_t layer);
+
+/*
+ * Step a4: fused norm -> RoPE -> KV append for B*T tokens of one layer.
+ *   q_in       [B][T][n_heads][head_dim]      raw q projections
+ *   k_in, v_in [B][T][n_kv_heads][head_dim]   raw k / v projections; must be
+ *              NULL on a shared layer (kv_share_src >= 0), non-NULL otherwise
+ *   q_norm_w   [head_dim] float32 weight shared by all q heads
+ *   k_norm_w   [head_dim] float32 weight shared by all k heads (NULL on a
+ *              shared layer).  v has no weight.
+ *   positions  [B][T] int32: the RoPE position of each token and the cache row
+ *              it is written to.  Rows outside [0, max_len) are not written.
+ *   q_out      [B][T][n_heads][head_dim] normed + roped q; may equal q_in.
+ * The layer's cache is caches[layer] (n_layers entries).  Writes exactly the
+ * rows k[b][*][positions[b][t]][*] and v[...] for every (b, t); nothing else
+ * in the cache changes.  RoPE angles are pos * inv_freq[j] with inv_freq held
+ * in float32 and the angle reduced in float64.
+ */
+g4_status g4_kv_append_normrope(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
+                                int32_t layer, const void* q_in, const void* k_in, const void* v_in,
+                                const float* q_norm_w, const float* k_norm_w, const int32_t* positions,
+                                int32_t B, int32_t T, void* q_out, void* stream);
+
+/*
+ * Step a5 (+ a7): prefill attention of T new tokens per sequence.
+ *   q            [B][T][n_heads][head_dim], normed + roped (g4_kv_append_normrope's q_out)
+ *   q_start_pos  [B] int32 device: token t of sequence b sits at position
+ *                q_start_pos[b] + t; the cache of the source layer must
+ *                already hold rows [0, q_start_pos[b] + T)
+ *   out          [B][T][n_heads][head_dim]
+ * Reads caches[src], src = kv_share_src < 0 ? layer : kv_share_src, which must
+ * match the layer's type, head_dim, n_kv_heads and dtype
+ * (G4_ERR_SHARE_MISMATCH otherwise).  bf16 runs on the tcgen05 tensor cores
+ * (bf16 operands, float32 accumulation, P rounded to bf16); f32 runs on CUDA
+ * cores in float32.
+ */
+g4_status g4_attn_prefill(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
+                          int32_t layer, const void* q, const int32_t* q_start_pos, int32_t B, int32_t T,
+                          void* out, void* stream);
+
+/*
+ * Workspace bytes g4_attn_decode needs for this layer, batch and bound on the
+ * sequence lengths (0 means no workspace is needed).
+ */
+size_t g4_attn_decode_workspace_size(const g4_layer_params* params, int32_t B, int32_t max_seq_len);
+
+/*
+ * Step a6 (+ a7): one query token per sequence (decode).
+ *   q            [B][n_heads][head_dim], normed + roped
+ *   seq_lens     [B] int32 device: keys per sequence INCLUDING the new token,
+ *                which sits at position seq_lens[b] - 1 (append it first).
+ *                Values are clamped into [1, max_seq_len].
+ *   max_seq_len  host-side upper bound of seq_lens, 1..cache max_len; it sizes
+ *                the split-KV grid and the workspace.
+ *   out          [B][n_heads][head_dim]
+ *   workspace    device scratch of at least g4_attn_decode_workspace_size()
+ *                bytes (may be NULL when that is 0); caller-owned, 16-byte
+ *                aligned, contents need no initialisation.
+ * Sliding layers read keys [max(0, L - window), L), full layers [0, L).  The
+ * key range is split across CTAs (split-KV) and merged with a log-sum-exp
+ * combine kernel.  Calls sharing a workspace must not overlap on the GPU.
+ */
+g4_status g4_attn_decode(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
+                         int32_t layer, const void* q, const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
+                         void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Thread-local message of the last non-OK status ("" if none). */
+const char* g4_last_error(void);
+
+/*
+ * Reads and clears the device-side error word (synchronises the device).
+ * Nonzero means a kernel gave up a bounded wait (code 1) and returned early;
+ * its outputs are then unspecified.  Returns -1 if the read itself failed.
+ */
+int32_t g4_take_device_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* G4ATTN_H */
