@@ -17,9 +17,9 @@
 //
 // Inside a warp, lane l owns HD/32 elements of every row (16-byte pieces
 // l, l+32, ... so shared-memory reads are conflict-free).  For a batch of
-// KB = 16/G keys the lane forms KB*G partial dot products with packed f32x2
-// FMAs, a butterfly reduce-scatter turns the 16 partials of 32 lanes into
-// 16 full scores, the scores go through shared memory so every lane holds
+// KB = min(16/G, 4 KB of rows) keys the lane forms KB*G partial dot products with packed f32x2
+// FMAs, a butterfly reduce-scatter turns the KB*G partials of 32 lanes into
+// KB*G full scores, the scores go through shared memory so every lane holds
 // all of them, and the online softmax (log2 domain; q is pre-scaled by
 // attn_scale*log2(e)) and the P.V update run redundantly per lane with no
 // further shuffles.  Warps merge their (m, l, o) at the end; with one split
@@ -35,12 +35,17 @@ namespace {
 
 constexpr int kNW = 4;   // warps per CTA
 constexpr int kNST = 3;  // stages per warp
-constexpr int kNP = 16;  // partial scores per reduce-scatter batch
+constexpr int kNPMax = 16;  // partial scores per reduce-scatter batch, at most
+constexpr int kStageMaxB = 4096;  // bytes of K (and of V) a reduce batch may span
 
-// Sum of v[i] over the 32 lanes, scattered: lane l returns the total of index l >> 1.
-__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
+constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+// Sum of v[i] over the 32 lanes, scattered: lane l returns the total of index
+// l >> (5 - log2(NP)).  NP is a power of two in [2, 32].
+template <int NP>
+__device__ __forceinline__ float reduce_scatter(float (&v)[NP], int lane) {
 #pragma unroll
-  for (int n = 16, o = 16; n > 1; n >>= 1, o >>= 1) {
+  for (int n = NP, o = 16; n > 1; n >>= 1, o >>= 1) {
     const bool up = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < n / 2; ++i) {
@@ -49,7 +54,10 @@ __device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
       v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
   }
-  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+  float r = v[0];
+#pragma unroll
+  for (int o = 16 >> ilog2(NP); o >= 1; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  return r;
 }
 
 template <typename T, int HD, int G>
@@ -59,15 +67,20 @@ struct SimtCfg {
   static constexpr int CHE = 16 / ES;                // elements per 16-byte piece
   static constexpr int PE = EL < CHE ? EL : CHE;     // elements per piece a lane reads
   static constexpr int NPC = EL / PE;                // pieces per lane per row
-  static constexpr int KB = kNP / G;                 // keys per reduce batch
   static constexpr int ROWB = HD * ES;               // bytes per cache row
+  static constexpr int KB_G = kNPMax / G;
+  static constexpr int KB_B = kStageMaxB / ROWB;
+  static constexpr int KB = KB_G < KB_B ? KB_G : KB_B;  // keys per reduce batch
+  static constexpr int NP = KB * G;                  // partial scores per batch (2..16)
   static constexpr int NB = (KB * ROWB >= 2048) ? 1 : 2048 / (KB * ROWB);  // batches per stage
   static constexpr int SK = KB * NB;                 // keys per stage
   static constexpr int STAGE_B = SK * ROWB;          // bytes of K (and of V) per stage
   static constexpr int RING_B = kNW * kNST * 2 * STAGE_B;
   static constexpr int MERGE_B = kNW * G * (HD + 2) * 4;
   static constexpr int AREA_B = RING_B > MERGE_B ? RING_B : MERGE_B;
-  static constexpr int SMEM_B = AREA_B + kNW * kNST * 8 + kNW * kNP * 4;
+  static constexpr int SMEM_B = AREA_B + kNW * kNST * 8 + kNW * kNPMax * 4;
+  static_assert(NP >= 2 && NP <= 16 && (NP & (NP - 1)) == 0, "reduce batch");
+  static_assert(SMEM_B <= 232448, "shared memory budget");
 };
 
 template <typename T, int NPC, int PE>
@@ -111,7 +124,7 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
 
   uint8_t* ring = smem + warp * (kNST * 2 * C::STAGE_B);
   uint64_t* wbar = bars + warp * kNST;
-  float* sc = sc_all + warp * kNP;
+  float* sc = sc_all + warp * kNPMax;
   bool aborted = false;
 
   if (lane == 0) {
@@ -182,7 +195,7 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
       const int kb0 = nb * C::KB;
       if (kb0 >= n) break;
       // Partial dot products: part[key * G + h].
-      float part[kNP];
+      float part[C::NP];
 #pragma unroll
       for (int key = 0; key < C::KB; ++key) {
         float2 kx[EL2];
@@ -195,15 +208,13 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
           part[key * G + h] = acc.x + acc.y;
         }
       }
-      const float s = reduce_scatter16(part, lane);
-      if ((lane & 1) == 0) sc[lane >> 1] = s;
+      constexpr int kSh = 5 - ilog2(C::NP);  // lanes sharing one reduced score: 1 << kSh
+      const float s = reduce_scatter<C::NP>(part, lane);
+      if ((lane & ((1 << kSh) - 1)) == 0) sc[lane >> kSh] = s;
       __syncwarp();
-      float sv_all[kNP];
+      float sv_all[C::NP];
 #pragma unroll
-      for (int i = 0; i < kNP / 4; ++i) {
-        const float4 v4 = reinterpret_cast<const float4*>(sc)[i];
-        sv_all[4 * i] = v4.x; sv_all[4 * i + 1] = v4.y; sv_all[4 * i + 2] = v4.z; sv_all[4 * i + 3] = v4.w;
-      }
+      for (int i = 0; i < C::NP; ++i) sv_all[i] = sc[i];
       __syncwarp();
       float p[C::KB][G];
 #pragma unroll

@@ -52,13 +52,20 @@ def bf16_ulp(x):
     return np.where(ax >= 2.0 ** -126, u, 2.0 ** -133)
 
 
+# Absolute slack of the float32 norm/rope arithmetic on values of order 1: a
+# rotated element that nearly cancels (|x'| ~ 1e-6) carries the ~1e-7 error of
+# its float32 products, which is more than one bf16 ulp of such a small value.
+STORE_ABS_SLACK = 1e-6
+
+
 def assert_stored_close(gpu, ref, dtype, what=""):
-    """Stored values of the append: bf16 within one ulp, f32 within 1e-4."""
+    """Stored values of the append, against the oracle's correctly rounded ones:
+    bf16 within one ulp (plus STORE_ABS_SLACK), f32 within 1e-4."""
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     assert np.all(np.isfinite(gpu)), what
     if dtype == W.BF16:
-        bad = np.abs(gpu - ref) > bf16_ulp(ref)
+        bad = np.abs(gpu - ref) > bf16_ulp(ref) + STORE_ABS_SLACK
         assert not bad.any(), f"{what}: {bad.sum()} values beyond 1 ulp, e.g. {gpu[bad][:4]} vs {ref[bad][:4]}"
     else:
         err = np.max(np.abs(gpu - ref)) if gpu.size else 0.0
@@ -74,7 +81,13 @@ def attn_errors(gpu, ref):
 
 
 def assert_attn_close(gpu, ref, dtype, what=""):
-    """Attention output tolerances: f32 max-abs 1e-4; bf16 max-abs 2e-2 and rel-L2 5e-3."""
+    """Attention output tolerances: f32 max-abs 1e-4; bf16 max-abs 2e-2 and rel-L2 5e-3.
+
+    ``ref`` is the oracle's exact (float64, unrounded) output, so the bound
+    covers the storage rounding of the stored value (half an ulp) plus the
+    computation error.  Comparing against a separately rounded reference
+    would count a full ulp (1/32 for |o| in [4, 8)) whenever the two land on
+    either side of a rounding boundary."""
     assert np.all(np.isfinite(np.asarray(gpu))), f"{what}: non-finite output"
     max_abs, rel_l2 = attn_errors(gpu, ref)
     if dtype == W.BF16:
@@ -157,8 +170,8 @@ class LayerRun:
         pos = self.positions()
         self.o_q = O.kv_append_normrope(lp, f64(self.x["q"]), f64(self.x["k"]), f64(self.x["v"]), qw, kw, pos, ck, cv)
         self.o_ck, self.o_cv = ck, cv
-        self.o_out = O.store(O.attention(self.o_q, ck, cv, pos, self.q_start + self.T, Hkv, g["layer_type"],
-                                         g["window"], g["attn_scale"]), g["dtype"])
+        self.o_out = O.attention(self.o_q, ck, cv, pos, self.q_start + self.T, Hkv, g["layer_type"],
+                                 g["window"], g["attn_scale"])
         return self
 
 
@@ -198,4 +211,4 @@ def run_decode(geo, lens, Lmax, seed, max_seq_len=None, decode_fn=None):
     oq = O.kv_append_normrope(lp, f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["qw"]), f64(x["kw"]),
                               (lens - 1)[:, None], ok, ov)
     ref = O.attention(oq, ok, ov, (lens - 1)[:, None], lens, Hkv, geo["layer_type"], geo["window"], 1.0)
-    return f64(out), O.store(ref[:, 0], dt), wsb
+    return f64(out), ref[:, 0], wsb
