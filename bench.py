@@ -1,0 +1,599 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention path: prefill attention tokens/s and decode KV
+GB/s against the GB300 roofline.
+
+Workload (default): the attention-only 42-layer stack -- 5 sliding : 1 full
+layers (sliding head_dim 256, window 512, theta 1e4; full head_dim 512, theta
+1e6, partial rotary 0.25), n_heads 8, n_kv 2, the last 18 layers shared-KV --
+at batch 8: prefill of T=4096 tokens, then 128 decode steps.  It is the one
+workload that runs every step of the path (norm/RoPE/append, sliding and full
+prefill attention, decode attention, shared-KV reads).  One benchmark step =
+the whole job: prefill of all 42 layers, then the 128 decode steps (captured
+in one CUDA graph).  Inputs are seeded N(0,1) bf16 drawn on the device; they
+total ~10 GB per step, far above the 129 MB L2, so no L2 flush is needed.
+
+value      prefill tokens/s: B*T / (prefill phase time).
+decode     KV GB/s: algorithmic bytes of the 128 decode steps / decode phase time.
+e2e        prefill tokens/s with the raw inputs copied host->device (pinned)
+           and the last layer's output copied back, every step.
+roofline   of the dominant kernel (most time per step), from CUDA events
+           around its launches inside the timed steps.
+cpu_baseline  the float64 oracle on one host core, on a bounded sample.
+
+  python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefill attn tokens/s and decode KV GB/s vs GB300 roofline, 1 GPU"
+WORKLOAD = "stack42_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DECODE_EVENT_STEPS = (0, 32, 64, 96, 127)
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- multi-process plumbing
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def reduce_max(x, device=None):
+    """Maximum of a float over all ranks (identity on one process)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x, device=None):
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", str(self.gpu_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- workload arithmetic
+
+def visible_pairs(T, window, sliding, q_start=0):
+    """Sum over the T queries of the keys each one sees (causal, window)."""
+    tot = 0
+    for i in range(q_start, q_start + T):
+        n = i + 1
+        tot += min(n, window) if sliding else n
+    return tot
+
+
+def prefill_flops(cfg, layer):
+    from gemma_dual_geometry_gb300 import workloads as W
+    g = W.layer_geometry(cfg, layer)
+    pairs = visible_pairs(cfg["T"], g["window"], g["layer_type"] == W.SLIDING)
+    return 4.0 * g["head_dim"] * cfg["H"] * cfg["B"] * pairs  # QK^T and PV, 2 flops per MAC
+
+
+def decode_bytes(cfg, layer, L):
+    """Algorithmic HBM bytes of one decode attention call at length L: the
+    visible K and V rows, the q read and the output write."""
+    from gemma_dual_geometry_gb300 import workloads as W
+    g = W.layer_geometry(cfg, layer)
+    keys = min(L, g["window"]) if g["layer_type"] == W.SLIDING else L
+    hd, B = g["head_dim"], cfg["B"]
+    return B * (keys * cfg["Hkv"] * hd * 2 * 2 + 2 * cfg["H"] * hd * 2)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- the GPU arm
+
+class Job:
+    """Device buffers and launch sequences of one benchmark step."""
+
+    def __init__(self, cfg, device):
+        import torch
+
+        from gemma_dual_geometry_gb300 import workloads as W
+        from gemma_dual_geometry_gb300.stack import AttnStack
+
+        self.cfg, self.W, self.torch = cfg, W, torch
+        self.B, self.T, self.S = cfg["B"], cfg["T"], cfg["decode_steps"]
+        self.Lmax = self.T + self.S
+        self.st = AttnStack(cfg, self.Lmax, device=device)
+        self.n = self.st.n
+        dev = device
+        H, Hkv, dt = cfg["H"], cfg["Hkv"], cfg["dtype"]
+        tdt = W.torch_dtype(dt)
+        hds = sorted({g["head_dim"] for g in self.st.geo})
+        # prefill inputs (raw projections) and decode inputs, per layer
+        self.X, self.D = [], []
+        for l in range(self.n):
+            owns = self.st.owns(l)
+            x = W.layer_inputs(cfg, l, self.T, owns, device=dev)
+            x["q_norm_w"] = x["q_norm_w"].to(dev)
+            if owns:
+                x["k_norm_w"] = x["k_norm_w"].to(dev)
+            self.X.append(x)
+            hd = self.st.geo[l]["head_dim"]
+            s = cfg["seed"]
+            d = dict(q=W.normal((self.S, self.B, 1, H, hd), W.seed_for(s, l, 7), dt, dev))
+            if owns:
+                d["k"] = W.normal((self.S, self.B, 1, Hkv, hd), W.seed_for(s, l, 8), dt, dev)
+                d["v"] = W.normal((self.S, self.B, 1, Hkv, hd), W.seed_for(s, l, 9), dt, dev)
+            self.D.append(d)
+        self.pos_pf = torch.arange(self.T, dtype=torch.int32, device=dev).repeat(self.B, 1).contiguous()
+        self.qs = torch.zeros(self.B, dtype=torch.int32, device=dev)
+        self.pos_dec = (self.T + torch.arange(self.S, dtype=torch.int32, device=dev))[:, None].repeat(1, self.B)
+        self.pos_dec = self.pos_dec.contiguous()
+        self.sl_dec = (self.pos_dec + 1).contiguous()
+        self.qo = {hd: torch.empty((self.B, self.T, H, hd), dtype=tdt, device=dev) for hd in hds}
+        self.out = {hd: torch.empty((self.B, self.T, H, hd), dtype=tdt, device=dev) for hd in hds}
+        self.qo_dec = {hd: torch.empty((self.B, 1, H, hd), dtype=tdt, device=dev) for hd in hds}
+        self.out_dec = {hd: torch.empty((self.B, H, hd), dtype=tdt, device=dev) for hd in hds}
+        self.full_layers = [l for l in range(self.n) if self.st.geo[l]["layer_type"] == W.FULL]
+        self.pf_events = []
+        self.dec_events = []
+        self.graph = None
+
+    # one pass of prefill over all layers
+    def prefill(self, record=False):
+        torch = self.torch
+        for l in range(self.n):
+            x, hd = self.X[l], self.st.geo[l]["head_dim"]
+            self.st.append(l, x["q"], x.get("k"), x.get("v"), x["q_norm_w"], x.get("k_norm_w"), self.pos_pf,
+                           self.T, self.qo[hd])
+            ev = None
+            if record and l in self.full_layers:
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ev[0].record()
+            self.st.prefill_attn(l, self.qo[hd], self.qs, self.T, self.out[hd])
+            if ev is not None:
+                ev[1].record()
+                self.pf_events.append(ev)
+
+    def decode(self, events=None):
+        H = self.cfg["H"]
+        for s in range(self.S):
+            for l in range(self.n):
+                d, hd = self.D[l], self.st.geo[l]["head_dim"]
+                self.st.append(l, d["q"][s], d["k"][s] if "k" in d else None, d["v"][s] if "v" in d else None,
+                               self.X[l]["q_norm_w"], self.X[l].get("k_norm_w"), self.pos_dec[s], 1, self.qo_dec[hd])
+                ev = events.get((s, l)) if events else None
+                if ev is not None:
+                    ev[0].record()
+                self.st.decode_attn(l, self.qo_dec[hd].view(self.B, H, hd), self.sl_dec[s], self.Lmax,
+                                    self.out_dec[hd])
+                if ev is not None:
+                    ev[1].record()
+
+    def capture_decode(self):
+        torch = self.torch
+        events = {}
+        try:
+            for s in DECODE_EVENT_STEPS:
+                for l in self.full_layers:
+                    events[(s, l)] = (torch.cuda.Event(enable_timing=True, external=True),
+                                      torch.cuda.Event(enable_timing=True, external=True))
+        except TypeError:
+            events = {}
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.decode()  # warm-up outside capture (attributes, symbol addresses)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.decode(events)
+        torch.cuda.synchronize()
+        self.dec_events = list(events.items())
+
+    def launches_per_step(self):
+        pf = 2 * self.n
+        dec = self.S * sum(1 + self.st.decode_launches(l) for l in range(self.n))
+        return pf + dec
+
+    def decode_step_bytes(self):
+        return sum(decode_bytes(self.cfg, l, self.T + s + 1) for s in range(self.S) for l in range(self.n))
+
+
+def run_ours(args, cfg):
+    import torch
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dist_init("nccl")
+    dev = torch.device("cuda", local)
+    from gemma_dual_geometry_gb300 import build as g4build
+    from gemma_dual_geometry_gb300 import g4attn as G
+    g4build.build()
+    G.lib()
+
+    job = Job(cfg, dev)
+    job.capture_decode()
+    B, T = cfg["B"], cfg["T"]
+
+    # warm-up
+    for _ in range(args.warmup):
+        job.prefill()
+        job.graph.replay()
+    torch.cuda.synchronize()
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_uuid = str(getattr(props, "uuid", "") or "")
+    if gpu_uuid and not gpu_uuid.startswith("GPU-"):
+        gpu_uuid = "GPU-" + gpu_uuid
+    clocks = ClockSampler(gpu_uuid)
+    ev_pf = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+              torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    job.pf_events = []
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_wall0 = time.perf_counter()
+    ev_all0 = torch.cuda.Event(enable_timing=True)
+    ev_all1 = torch.cuda.Event(enable_timing=True)
+    ev_all0.record()
+    dec_samples = []
+    for i in range(args.steps):
+        ev_pf[i][0].record()
+        job.prefill(record=True)
+        ev_pf[i][1].record()
+        job.graph.replay()
+        ev_pf[i][2].record()
+        if job.dec_events and i == args.steps - 1:
+            pass
+    ev_all1.record()
+    torch.cuda.synchronize()
+    barrier()
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    # decode kernel events hold the last replay's timings
+    for (s, l), (e0, e1) in job.dec_events:
+        dec_samples.append((s, l, e0.elapsed_time(e1) * 1e-3))
+
+    total_s = ev_all0.elapsed_time(ev_all1) * 1e-3
+    pf_s = sum(e[0].elapsed_time(e[1]) for e in ev_pf) * 1e-3
+    dec_s = sum(e[1].elapsed_time(e[2]) for e in ev_pf) * 1e-3
+    total_s = reduce_max(total_s, dev)
+    pf_s = reduce_max(pf_s, dev)
+    dec_s = reduce_max(dec_s, dev)
+
+    tokens = B * T * args.steps * world
+    value = tokens / pf_s
+    dec_bytes = job.decode_step_bytes()
+    dec_gbs = dec_bytes * args.steps * world / dec_s / 1e9
+
+    peaks, peak_src = load_peaks()
+    # prefill dominant kernel: tcgen05 attention of the full layers
+    pf_launch = [e[0].elapsed_time(e[1]) * 1e-3 for e in job.pf_events]
+    fl = job.full_layers[0]
+    pf_flops = prefill_flops(cfg, fl)
+    pf_avg = statistics.mean(pf_launch)
+    rl_prefill = dict(kernel="prefill_tc_kernel<512> (full layer, tcgen05)", bound="tensor",
+                      achieved=pf_flops / pf_avg / 1e12, peak=peaks["bf16_tflops_sustained"], unit="TFLOP/s",
+                      peak_kind=f"{peak_src} bf16 dense, sustained (timed inside a long step)",
+                      flops_per_launch=pf_flops, avg_launch_ms=pf_avg * 1e3, launches_sampled=len(pf_launch),
+                      launches_per_step=len(job.full_layers), traffic=None)
+    rl_prefill["frac"] = rl_prefill["achieved"] / rl_prefill["peak"]
+    rooflines = [rl_prefill]
+    if dec_samples:
+        per = [decode_bytes(cfg, l, T + s + 1) / t for (s, l, t) in dec_samples]
+        avg_t = statistics.mean(t for (_, _, t) in dec_samples)
+        avg_b = statistics.mean(decode_bytes(cfg, l, T + s + 1) for (s, l, _) in dec_samples)
+        rl_dec = dict(kernel="attn_simt_kernel<bf16,512,4> + combine (full-layer decode, split-KV)", bound="hbm",
+                      achieved=avg_b / avg_t / 1e9, peak=peaks["hbm_gbs"], unit="GB/s",
+                      peak_kind=f"{peak_src} HBM copy bandwidth", bytes_per_launch=avg_b,
+                      avg_launch_ms=avg_t * 1e3, launches_sampled=len(dec_samples),
+                      launches_per_step=len(job.full_layers) * cfg["decode_steps"], traffic=None,
+                      per_launch_gbs_min=min(per) / 1e9, per_launch_gbs_max=max(per) / 1e9)
+        rl_dec["frac"] = rl_dec["achieved"] / rl_dec["peak"]
+        rooflines.append(rl_dec)
+    # the dominant kernel is the one with the most time per step
+    dominant = max(rooflines, key=lambda r: r["avg_launch_ms"] * r["launches_per_step"])
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), on device)",
+        "config": {"workload": "attention-only 42-layer stack (5 sliding : 1 full, last 18 shared-KV), "
+                               "n_heads 8, n_kv 2, head_dim 256 / global 512, window 512, batch 8 per GPU, "
+                               "prefill T=4096 then 128 decode steps",
+                   "global_batch": B * world, "seq_len": T, "decode_steps": cfg["decode_steps"],
+                   "parallelism": f"replicas x{world} (independent sequences, no collective)",
+                   "l2": "inputs larger than L2 (~10 GB per step), no flush",
+                   "value_definition": "B*T prefill tokens / prefill-phase time (CUDA events)"},
+        "ms_prefill_per_step": pf_s / args.steps * 1e3, "ms_decode_per_step": dec_s / args.steps * 1e3,
+        "decode": {"value": dec_gbs, "unit": "GB/s", "frac_of_hbm": dec_gbs / peaks["hbm_gbs"],
+                   "bytes_per_step": dec_bytes, "note": "algorithmic KV + q + out bytes of 128 steps x 42 layers "
+                                                         "/ decode-phase time (one CUDA graph)"},
+        "roofline": dominant, "rooflines": rooflines,
+        "gpu_launches": job.launches_per_step() * args.steps, "clocks": clk,
+        "wall_s_timed_region": t_wall,
+    }
+
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(job, args, dev, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, steps=1, warmup=0)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(job, args, dev, world):
+    """Prefill through the public API with the step's raw inputs copied in from
+    pinned host memory and the last layer's output copied back, every step."""
+    import torch
+    host = []
+    h2d = 0
+    for x in job.X:
+        hx = {}
+        for k in ("q", "k", "v"):
+            if k in x:
+                h = torch.empty(x[k].shape, dtype=x[k].dtype, pin_memory=True)
+                h.copy_(x[k])
+                hx[k] = h
+                h2d += h.numel() * h.element_size()
+        host.append(hx)
+    last_hd = job.st.geo[job.n - 1]["head_dim"]
+    out_h = torch.empty(job.out[last_hd].shape, dtype=job.out[last_hd].dtype, pin_memory=True)
+    d2h = out_h.numel() * out_h.element_size()
+    steps = max(1, args.e2e_steps)
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record()
+    for _ in range(steps):
+        for x, hx in zip(job.X, host):
+            for k, h in hx.items():
+                x[k].copy_(h, non_blocking=True)
+        job.prefill()
+        out_h.copy_(job.out[last_hd], non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    dt = reduce_max(e0.elapsed_time(e1) * 1e-3, dev)
+    tokens = job.B * job.T * steps * world
+    return {"value": tokens / dt, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps, "wall_s": wall, "what": "prefill of the 42-layer stack; inputs H2D from pinned host "
+                                                     "memory and the last layer's output D2H inside the timed region"}
+
+
+# ---------------------------------------------------------------- the oracle (CPU) arm
+
+def oracle_worker(spec):
+    """Runs in a subprocess with one BLAS thread: the float64 oracle on a bounded
+    sample of the stack workload.  Per layer, sequence 0: the append (norm/RoPE
+    of q, k, v) of a chunk of tokens and attention for sampled query tokens (all
+    heads) over the full-length cache.  Cost per token = append time per token
+    + attention time per query token; tokens/s is its inverse."""
+    import numpy as np
+
+    from gemma_dual_geometry_gb300 import workloads as W
+    from oracle import g4_oracle as O
+
+    cfg = W.CONFIGS[spec["workload"]]
+    T, H, Hkv = cfg["T"], cfg["H"], cfg["Hkv"]
+    n = len(cfg["types"])
+    nq, chunk = spec["n_query"], spec["append_chunk"]
+    is_s = [t == W.SLIDING for t in cfg["types"]]
+    src = [O.kv_share_src(n, cfg["n_shared"], is_s, l) for l in range(n)]
+    tq = np.linspace(0, T - 1, nq).astype(np.int64)
+
+    def f64(t):
+        return t.double().numpy()
+
+    # setup (untimed): sequence 0's raw inputs for the appended chunk and the
+    # sampled query tokens, and full-length caches of the owning layers
+    # (seeded N(0,1) rows; the attention cost does not depend on the values,
+    # and the append is timed on its own below)
+    caches, inputs = {}, {}
+    for l in range(n):
+        x = {k: f64(v) for k, v in W.layer_inputs(cfg, l, chunk, src[l] < 0, B=1).items()}
+        hd = W.layer_geometry(cfg, l)["head_dim"]
+        x["q_sampled"] = f64(W.normal((1, nq, H, hd), W.seed_for(cfg["seed"], l, 10), cfg["dtype"]))
+        inputs[l] = x
+        if src[l] < 0:
+            ck, cv = W.prefilled_cache(cfg, l, T, B=1)
+            caches[l] = (f64(ck), f64(cv))
+    steps = []
+    for _ in range(spec["warmup"] + spec["steps"]):
+        t_app = t_att = 0.0
+        for l in range(n):
+            geo, x = W.layer_geometry(cfg, l), inputs[l]
+            lp = dict(geo, kv_share_src=src[l])
+            s_l = l if src[l] < 0 else src[l]
+            ck, cv = caches[s_l]
+            t0 = time.perf_counter()
+            pos = np.arange(chunk)[None, :]
+            O.kv_append_normrope(lp, x["q"], x.get("k"), x.get("v"), x["q_norm_w"], x.get("k_norm_w"), pos,
+                                 ck if src[l] < 0 else None, cv if src[l] < 0 else None)
+            t1 = time.perf_counter()
+            qn = O.store(O.normrope_q(x["q_sampled"], x["q_norm_w"], tq[None, :], geo["head_dim"], geo["theta"],
+                                      geo["rotary_fraction"], geo["eps"]), geo["dtype"])
+            rows = [(0, i, h) for i in range(nq) for h in range(H)]
+            O.attention_rows(qn, ck, cv, rows, tq[None, :], [T], Hkv, geo["layer_type"], geo["window"],
+                             geo["attn_scale"])
+            t2 = time.perf_counter()
+            t_app += t1 - t0
+            t_att += t2 - t1
+        steps.append(dict(t_append=t_app, t_attn=t_att, per_token_s=t_app / chunk + t_att / nq))
+    return steps[spec["warmup"]:]
+
+
+def _oracle_subprocess(workload, steps, warmup, n_query=16, append_chunk=256):
+    spec = dict(workload=workload, steps=steps, warmup=warmup, n_query=n_query, append_chunk=append_chunk)
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[k] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    t0 = time.perf_counter()
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker", json.dumps(spec)],
+                       capture_output=True, text=True, env=env)
+    if r.returncode != 0:
+        raise RuntimeError("oracle worker failed: " + r.stderr[-2000:])
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    return res, time.perf_counter() - t0, spec
+
+
+def cpu_baseline(workload, steps=1, warmup=0):
+    res, wall, spec = _oracle_subprocess(workload, steps, warmup)
+    per = statistics.median(s["per_token_s"] for s in res)
+    return {"value": 1.0 / per, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"sequence 0 of the stack: per layer, append of {spec['append_chunk']} tokens and attention "
+                      f"for {spec['n_query']} evenly spaced query tokens x 8 heads over the 4096-token cache; "
+                      f"tokens/s = 1 / (append s/token + attention s/query token); numpy float64, one BLAS thread",
+            "wall_s": wall}
+
+
+def run_reference(args, cfg):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    res, wall, spec = _oracle_subprocess(args.workload, args.steps, args.warmup)
+    per = [s["per_token_s"] for s in res]
+    value = 1.0 / statistics.median(per)
+    step_s = statistics.mean(s["t_append"] + s["t_attn"] for s in res)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded N(0,1))",
+        "config": {"workload": "attention-only 42-layer stack (5 sliding : 1 full, last 18 shared-KV), "
+                               "n_heads 8, n_kv 2, head_dim 256 / global 512, window 512, batch 8, "
+                               "prefill T=4096 then 128 decode steps", "global_batch": cfg["B"],
+                   "seq_len": cfg["T"], "parallelism": "single host core"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"per step: sequence 0, per layer append of {spec['append_chunk']} tokens and "
+                                   f"attention for {spec['n_query']} query tokens x 8 heads (float64 oracle)"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": wall,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.oracle_worker:
+        res = oracle_worker(json.loads(args.oracle_worker))
+        print(json.dumps(res), flush=True)
+        return
+    from gemma_dual_geometry_gb300 import workloads as W
+    cfg = W.CONFIGS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()
