@@ -6,6 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
 #include <string>
 
 #include "../../include/g4attn.h"
@@ -105,6 +106,34 @@ g4_status resolve_src(const g4_layer_params* p, const g4_kv_cache* caches, int n
 g4_status cuda_status(cudaError_t e, const char* what) {
   if (e == cudaSuccess) return ok();
   return fail(G4_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Scratch for g4_attn_decode_noalloc: a fixed array in device global memory,
+// created when the library's device code is loaded on a GPU and held until the
+// process exits.  Host code must not hand `g_noalloc_scratch` itself to a
+// kernel (on the host it only names the symbol); noalloc_scratch() looks up
+// its device address once per device.
+constexpr size_t kNoAllocScratchBytes = G4_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+void* noalloc_scratch(cudaError_t* e) {
+  static std::mutex mu;
+  static void* addr[128] = {};
+  int dev = 0;
+  *e = cudaGetDevice(&dev);
+  if (*e != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= 128) {
+    *e = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    *e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // with this device current
+    if (*e != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
 }
 
 }  // namespace
@@ -306,6 +335,31 @@ g4_status g4_attn_decode(const g4_layer_params* params, const g4_kv_cache* cache
   st = cuda_status(g4::launch_attn_simt(a, params->dtype, s), "decode launch");
   if (st != G4_OK || plan.nsplit <= 1) return st;
   return cuda_status(g4::launch_attn_combine(a, params->dtype, s), "decode combine launch");
+}
+
+g4_status g4_attn_decode_noalloc(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
+                                 int32_t layer, const void* q, const int32_t* seq_lens, int32_t B,
+                                 int32_t max_seq_len, void* out, void* stream) {
+  g4_status st = check_params(params);
+  if (st != G4_OK) return st;
+  if (B >= 1 && max_seq_len >= 1) {
+    const g4::DecodePlan plan = g4::decode_plan(params->layer_type == G4_SLIDING, params->window,
+                                                params->head_dim, params->n_heads, params->n_kv_heads, B,
+                                                max_seq_len);
+    if (plan.ws_bytes > kNoAllocScratchBytes)
+      return fail(G4_ERR_WORKSPACE,
+                  "this decode needs %zu bytes of scratch, more than the %zu bytes built into the library for "
+                  "g4_attn_decode_noalloc; call g4_attn_decode with a caller-allocated workspace instead",
+                  plan.ws_bytes, kNoAllocScratchBytes);
+  }
+  cudaError_t e = cudaSuccess;
+  void* scratch = noalloc_scratch(&e);
+  if (scratch == nullptr) return fail(G4_ERR_CUDA, "cannot resolve the built-in decode scratch: %s", cudaGetErrorString(e));
+  // Same kernels and split plan as g4_attn_decode; the split partials go to
+  // the built-in array.  Every partial a call's combine reads is written by
+  // that call's split kernel first, so nothing needs clearing between calls.
+  return g4_attn_decode(params, caches, n_layers, layer, q, seq_lens, B, max_seq_len, out, scratch,
+                        kNoAllocScratchBytes, stream);
 }
 
 const char* g4_last_error(void) { return g_last_error.c_str(); }

@@ -52,6 +52,8 @@ SIGNATURES = {
     "g4_attn_decode_workspace_size": (ctypes.c_size_t, [_P(G4LayerParams), _i32, _i32]),
     "g4_attn_decode": (_i32, [_P(G4LayerParams), _P(G4KVCache), _i32, _i32, _c_void_p, _c_void_p, _i32, _i32,
                               _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p]),
+    "g4_attn_decode_noalloc": (_i32, [_P(G4LayerParams), _P(G4KVCache), _i32, _i32, _c_void_p, _c_void_p, _i32,
+                                      _i32, _c_void_p, _c_void_p]),
     "g4_last_error": (ctypes.c_char_p, []),
     "g4_take_device_error": (_i32, []),
 }
@@ -144,6 +146,15 @@ def g4_attn_decode(params, caches, layer, q, seq_lens, B, max_seq_len, out, work
                    stream=None):
     _check(lib().g4_attn_decode(ctypes.byref(params), caches, len(caches), layer, _ptr(q), _ptr(seq_lens), B,
                                 max_seq_len, _ptr(out), _ptr(workspace), int(workspace_bytes), _stream(stream, q)))
+
+
+G4_NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def g4_attn_decode_noalloc(params, caches, layer, q, seq_lens, B, max_seq_len, out, stream=None):
+    """g4_attn_decode with the library's built-in scratch instead of a workspace."""
+    _check(lib().g4_attn_decode_noalloc(ctypes.byref(params), caches, len(caches), layer, _ptr(q), _ptr(seq_lens),
+                                        B, max_seq_len, _ptr(out), _stream(stream, q)))
 
 
 def g4_last_error():

@@ -196,6 +196,37 @@ g4_status g4_attn_decode(const g4_layer_params* params, const g4_kv_cache* cache
                          int32_t layer, const void* q, const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
                          void* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Bytes of device scratch built into the library for g4_attn_decode_noalloc
+ * (16 MiB).  Every GPU that loads the library holds this array until the
+ * process exits.
+ */
+#define G4_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * g4_attn_decode without a workspace argument, for callers that cannot
+ * allocate device memory: code that is handed only its input and output
+ * buffers (a plugin or custom op inside a host framework that owns every
+ * allocation), or a serving loop that must not call cudaMalloc because it
+ * synchronises the device and can fail mid-request.  (The pages have no
+ * counterpart: this is an interface choice of this library.)
+ *
+ * Arguments, results and error codes are those of g4_attn_decode; the
+ * split-KV partials go to a fixed array of G4_NOALLOC_SCRATCH_BYTES inside
+ * the library instead of a caller's workspace.  A call whose split plan
+ * (g4_attn_decode_workspace_size) exceeds that size returns
+ * G4_ERR_WORKSPACE and launches nothing.  The call allocates nothing.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array and it keeps the last call's
+ * contents: calls whose kernels overlap on the GPU (different streams, or
+ * several threads) race on it and must be serialised by the caller.
+ */
+g4_status g4_attn_decode_noalloc(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
+                                 int32_t layer, const void* q, const int32_t* seq_lens, int32_t B,
+                                 int32_t max_seq_len, void* out, void* stream);
+
 /* Thread-local message of the last non-OK status ("" if none). */
 const char* g4_last_error(void);
 
