@@ -428,6 +428,145 @@ def run_ours(args, cfg):
         print(json.dumps(line), flush=True)
 
 
+class LayerJob:
+    """One- or two-layer workloads: single-layer prefill (prefill_bf16) or
+    decode against prefilled caches (decode_bf16, longctx_decode_bf16).  A step
+    is append + attention for every layer of the workload."""
+
+    def __init__(self, cfg, device):
+        import torch
+
+        from gemma_dual_geometry_gb300 import workloads as W
+        from gemma_dual_geometry_gb300.stack import AttnStack
+
+        self.cfg, self.W, self.torch = cfg, W, torch
+        self.B = cfg["B"]
+        self.decode = "T" not in cfg
+        H, Hkv, dt = cfg["H"], cfg["Hkv"], cfg["dtype"]
+        if self.decode:
+            if "L" in cfg:
+                self.L = [cfg["L"]] * self.B
+            else:
+                self.L = [int(x) for x in W.lengths(self.B, cfg["L_lo"], cfg["L_hi"], cfg["seed"])]
+            self.Lmax = max(self.L)
+            self.T = 1
+        else:
+            self.T = cfg["T"]
+            self.Lmax = self.T
+        self.st = AttnStack(cfg, self.Lmax, device=device)
+        self.n = self.st.n
+        if self.decode:
+            for l in range(self.n):
+                k, v = W.prefilled_cache(cfg, l, self.Lmax, device=device)
+                self.st.caches[l][0].copy_(k)
+                self.st.caches[l][1].copy_(v)
+                del k, v
+        self.X = []
+        for l in range(self.n):
+            x = W.layer_inputs(cfg, l, self.T, True, device=device)
+            x["q_norm_w"] = x["q_norm_w"].to(device)
+            x["k_norm_w"] = x["k_norm_w"].to(device)
+            self.X.append(x)
+        if self.decode:
+            self.pos = torch.tensor([[L - 1] for L in self.L], dtype=torch.int32, device=device)
+            self.sl = torch.tensor(self.L, dtype=torch.int32, device=device)
+        else:
+            self.pos = torch.arange(self.T, dtype=torch.int32, device=device).repeat(self.B, 1).contiguous()
+            self.qs = torch.zeros(self.B, dtype=torch.int32, device=device)
+        self.qo = [torch.empty_like(x["q"]) for x in self.X]
+        self.out = [torch.empty_like(x["q"]) for x in self.X]
+        self.events = {l: [] for l in range(self.n)}
+
+    def step(self, record=False):
+        torch = self.torch
+        H = self.cfg["H"]
+        for l in range(self.n):
+            x, hd = self.X[l], self.st.geo[l]["head_dim"]
+            self.st.append(l, x["q"], x["k"], x["v"], x["q_norm_w"], x["k_norm_w"], self.pos, self.T, self.qo[l])
+            ev = None
+            if record:
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ev[0].record()
+            if self.decode:
+                self.st.decode_attn(l, self.qo[l].view(self.B, H, hd), self.sl, self.Lmax,
+                                    self.out[l].view(self.B, H, hd))
+            else:
+                self.st.prefill_attn(l, self.qo[l], self.qs, self.T, self.out[l])
+            if ev is not None:
+                ev[1].record()
+                self.events[l].append(ev)
+
+    def layer_work(self, l):
+        """Algorithmic flops (prefill) or bytes (decode) of one attention launch of layer l."""
+        if self.decode:
+            return sum(decode_bytes(dict(self.cfg, B=1), l, L) for L in self.L)
+        return prefill_flops(self.cfg, l)
+
+    def launches_per_step(self):
+        if self.decode:
+            return sum(1 + self.st.decode_launches(l) for l in range(self.n))
+        return 2 * self.n
+
+
+def run_layers(args, cfg):
+    import torch
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dist_init("nccl")
+    dev = torch.device("cuda", local)
+    from gemma_dual_geometry_gb300 import build as g4build
+    from gemma_dual_geometry_gb300 import g4attn as G
+    g4build.build()
+    G.lib()
+    job = LayerJob(cfg, dev)
+    for _ in range(args.warmup):
+        job.step()
+    torch.cuda.synchronize()
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        job.step(record=True)
+    e1.record()
+    torch.cuda.synchronize()
+    barrier()
+    total = reduce_max(e0.elapsed_time(e1) * 1e-3, dev)
+    peaks, src = load_peaks()
+    per_layer = []
+    for l in range(job.n):
+        t = statistics.mean(a.elapsed_time(b) for a, b in job.events[l]) * 1e-3
+        w = job.layer_work(l)
+        g = job.st.geo[l]
+        if job.decode:
+            ach, peak, unit, bound = w / t / 1e9, peaks["hbm_gbs"], "GB/s", "hbm"
+        else:
+            ach, peak, unit, bound = w / t / 1e12, peaks["bf16_tflops"], "TFLOP/s", "tensor"
+        per_layer.append(dict(layer=l, layer_type="sliding" if g["layer_type"] == 0 else "full",
+                              head_dim=g["head_dim"], bound=bound, achieved=ach, peak=peak, unit=unit,
+                              frac=ach / peak, avg_launch_ms=t * 1e3, work_per_launch=w, traffic=None,
+                              peak_kind=f"{src} " + ("HBM copy" if job.decode else "bf16 dense, burst (kernel timed alone)")))
+    dominant = max(per_layer, key=lambda r: r["avg_launch_ms"])
+    if job.decode:
+        step_bytes = sum(job.layer_work(l) for l in range(job.n))
+        value, unit = step_bytes * args.steps * world / total / 1e9, "GB/s"
+        what = f"B={job.B} decode, lengths {min(job.L)}..{max(job.L)}"
+    else:
+        value, unit = job.B * job.T * args.steps * world / total, "tokens/s"
+        what = f"B={job.B} prefill, T={job.T}"
+    line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), on device)",
+            "config": {"workload": f"{args.workload}: {what}, layers " +
+                                   ", ".join(f"{r['layer_type']} hd {r['head_dim']}" for r in per_layer)},
+            "roofline": dominant, "rooflines": per_layer,
+            "gpu_launches": job.launches_per_step() * args.steps}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_e2e(job, args, dev, world):
     """Prefill through the public API with the step's raw inputs copied in from
     pinned host memory and the last layer's output copied back, every step."""
@@ -591,8 +730,10 @@ def main():
     cfg = W.CONFIGS[args.workload]
     if args.impl == "reference":
         run_reference(args, cfg)
-    else:
+    elif "decode_steps" in cfg:
         run_ours(args, cfg)
+    else:
+        run_layers(args, cfg)
 
 
 if __name__ == "__main__":
