@@ -258,16 +258,17 @@ class Job:
                 self.pf_events.append(ev)
 
     def decode(self, events=None):
-        H = self.cfg["H"]
+        H, Hkv = self.cfg["H"], self.cfg["Hkv"]
         for s in range(self.S):
             for l in range(self.n):
                 d, hd = self.D[l], self.st.geo[l]["head_dim"]
-                self.st.append(l, d["q"][s], d["k"][s] if "k" in d else None, d["v"][s] if "v" in d else None,
-                               self.X[l]["q_norm_w"], self.X[l].get("k_norm_w"), self.pos_dec[s], 1, self.qo_dec[hd])
                 ev = events.get((s, l)) if events else None
                 if ev is not None:
                     ev[0].record()
-                self.st.decode_attn(l, self.qo_dec[hd].view(self.B, H, hd), self.sl_dec[s], self.Lmax,
+                self.st.decode_step(l, d["q"][s].view(self.B, H, hd),
+                                    d["k"][s].view(self.B, Hkv, hd) if "k" in d else None,
+                                    d["v"][s].view(self.B, Hkv, hd) if "v" in d else None,
+                                    self.X[l]["q_norm_w"], self.X[l].get("k_norm_w"), self.sl_dec[s], self.Lmax,
                                     self.out_dec[hd])
                 if ev is not None:
                     ev[1].record()
@@ -296,7 +297,7 @@ class Job:
 
     def launches_per_step(self):
         pf = 2 * self.n
-        dec = self.S * sum(1 + self.st.decode_launches(l) for l in range(self.n))
+        dec = self.S * sum(self.st.decode_launches(l) for l in range(self.n))
         return pf + dec
 
     def decode_step_bytes(self):
@@ -389,7 +390,8 @@ def run_ours(args, cfg):
         per = [decode_bytes(cfg, l, T + s + 1) / t for (s, l, t) in dec_samples]
         avg_t = statistics.mean(t for (_, _, t) in dec_samples)
         avg_b = statistics.mean(decode_bytes(cfg, l, T + s + 1) for (s, l, _) in dec_samples)
-        rl_dec = dict(kernel="attn_simt_kernel<bf16,512,4> + combine (full-layer decode, split-KV)", bound="hbm",
+        rl_dec = dict(kernel="attn_simt_kernel<bf16,512,4,fused> (full-layer decode step: append + split-KV "
+                             "attention + last-CTA merge)", bound="hbm",
                       achieved=avg_b / avg_t / 1e9, peak=peaks["hbm_gbs"], unit="GB/s",
                       peak_kind=f"{peak_src} HBM copy bandwidth", bytes_per_launch=avg_b,
                       avg_launch_ms=avg_t * 1e3, launches_sampled=len(dec_samples),
@@ -414,7 +416,7 @@ def run_ours(args, cfg):
         "ms_prefill_per_step": pf_s / args.steps * 1e3, "ms_decode_per_step": dec_s / args.steps * 1e3,
         "decode": {"value": dec_gbs, "unit": "GB/s", "frac_of_hbm": dec_gbs / peaks["hbm_gbs"],
                    "bytes_per_step": dec_bytes, "note": "algorithmic KV + q + out bytes of 128 steps x 42 layers "
-                                                         "/ decode-phase time (one CUDA graph)"},
+                                                         "/ decode-phase time (one CUDA graph of fused decode steps)"},
         "roofline": dominant, "rooflines": rooflines,
         "gpu_launches": job.launches_per_step() * args.steps, "clocks": clk,
         "wall_s_timed_region": t_wall,
@@ -479,16 +481,19 @@ class LayerJob:
 
     def step(self, record=False):
         torch = self.torch
-        H = self.cfg["H"]
+        H, Hkv = self.cfg["H"], self.cfg["Hkv"]
         for l in range(self.n):
             x, hd = self.X[l], self.st.geo[l]["head_dim"]
-            self.st.append(l, x["q"], x["k"], x["v"], x["q_norm_w"], x["k_norm_w"], self.pos, self.T, self.qo[l])
+            if not self.decode:
+                self.st.append(l, x["q"], x["k"], x["v"], x["q_norm_w"], x["k_norm_w"], self.pos, self.T,
+                               self.qo[l])
             ev = None
             if record:
                 ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 ev[0].record()
             if self.decode:
-                self.st.decode_attn(l, self.qo[l].view(self.B, H, hd), self.sl, self.Lmax,
+                self.st.decode_step(l, x["q"].view(self.B, H, hd), x["k"].view(self.B, Hkv, hd),
+                                    x["v"].view(self.B, Hkv, hd), x["q_norm_w"], x["k_norm_w"], self.sl, self.Lmax,
                                     self.out[l].view(self.B, H, hd))
             else:
                 self.st.prefill_attn(l, self.qo[l], self.qs, self.T, self.out[l])
@@ -504,7 +509,7 @@ class LayerJob:
 
     def launches_per_step(self):
         if self.decode:
-            return sum(1 + self.st.decode_launches(l) for l in range(self.n))
+            return sum(self.st.decode_launches(l) for l in range(self.n))
         return 2 * self.n
 
 

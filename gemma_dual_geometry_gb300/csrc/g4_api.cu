@@ -277,15 +277,35 @@ size_t g4_attn_decode_workspace_size(const g4_layer_params* params, int32_t B, i
       .ws_bytes;
 }
 
-g4_status g4_attn_decode(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers, int32_t layer,
-                         const void* q, const int32_t* seq_lens, int32_t B, int32_t max_seq_len, void* out,
-                         void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by g4_attn_decode and g4_decode_step: validation, split plan and launch.
+// q is normed+roped (fused == false) or the raw projection (fused == true, with
+// k_in / v_in / weights and the RoPE table of the layer).
+g4_status decode_common(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers, int32_t layer,
+                        const void* q, const void* k_in, const void* v_in, const float* q_norm_w,
+                        const float* k_norm_w, bool fused, const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
+                        void* out, void* workspace, size_t workspace_bytes, void* stream) {
   g4_status st = check_params(params);
   if (st != G4_OK) return st;
   if (B < 0) return fail(G4_ERR_INVALID_ARG, "B %d must be >= 0", B);
   if (q == nullptr || out == nullptr || seq_lens == nullptr)
     return fail(G4_ERR_INVALID_ARG, "q, out and seq_lens must be non-NULL");
   if (!aligned16(q) || !aligned16(out)) return fail(G4_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  const bool shared = params->kv_share_src >= 0;
+  if (fused) {
+    if (q_norm_w == nullptr || !aligned16(q_norm_w))
+      return fail(G4_ERR_INVALID_ARG, "q_norm_w must be non-NULL and 16-byte aligned");
+    if (shared && (k_in != nullptr || v_in != nullptr || k_norm_w != nullptr))
+      return fail(G4_ERR_INVALID_ARG, "layer %d shares the cache of layer %d: k_in, v_in and k_norm_w must be NULL",
+                  layer, params->kv_share_src);
+    if (!shared && (k_in == nullptr || v_in == nullptr || k_norm_w == nullptr))
+      return fail(G4_ERR_INVALID_ARG, "layer %d owns its cache: k_in, v_in and k_norm_w must be non-NULL", layer);
+    if (!shared && (!aligned16(k_in) || !aligned16(v_in) || !aligned16(k_norm_w)))
+      return fail(G4_ERR_INVALID_ARG, "k_in, v_in and k_norm_w must be 16-byte aligned");
+  }
   const g4_kv_cache* c = nullptr;
   st = resolve_src(params, caches, n_layers, layer, &c);
   if (st != G4_OK) return st;
@@ -323,18 +343,52 @@ g4_status g4_attn_decode(const g4_layer_params* params, const g4_kv_cache* cache
   a.nsplit = plan.nsplit;
   a.scale_log2 = params->attn_scale * 1.4426950408889634f;
   if (plan.nsplit > 1) {
-    const size_t np = static_cast<size_t>(B) * a.H * plan.nsplit;
-    const size_t o_b = (np * a.hd * 4 + 255) / 256 * 256;
-    const size_t m_b = (np * 4 + 255) / 256 * 256;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.ws_o = reinterpret_cast<float*>(ws);
-    a.ws_m = reinterpret_cast<float*>(ws + o_b);
-    a.ws_l = reinterpret_cast<float*>(ws + o_b + m_b);
+    a.ws_m = reinterpret_cast<float*>(ws + plan.o_bytes);
+    a.ws_l = reinterpret_cast<float*>(ws + plan.o_bytes + plan.m_bytes);
+    a.tickets = reinterpret_cast<unsigned*>(ws + plan.o_bytes + 2 * plan.m_bytes);
   }
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = cuda_status(g4::launch_attn_simt(a, params->dtype, s), "decode launch");
-  if (st != G4_OK || plan.nsplit <= 1) return st;
-  return cuda_status(g4::launch_attn_combine(a, params->dtype, s), "decode combine launch");
+  if (fused) {
+    a.fused = 1;
+    a.q_w = q_norm_w;
+    a.eps = params->eps;
+    if (!shared) {
+      a.k_raw = k_in;
+      a.v_raw = v_in;
+      a.k_w = k_norm_w;
+      a.cache_k = caches[layer].k;
+      a.cache_v = caches[layer].v;
+    }
+    const int half = a.hd / 2;
+    int n_rot =
+        static_cast<int>(floor(static_cast<double>(a.hd) * static_cast<double>(params->rotary_fraction) / 2.0));
+    if (n_rot > half) n_rot = half;
+    a.n_rot = n_rot;
+    for (int j = 0; j < half; ++j)
+      a.inv_freq[j] =
+          j < n_rot ? static_cast<float>(pow(static_cast<double>(params->theta), -2.0 * j / a.hd)) : 0.0f;
+  }
+  return cuda_status(g4::launch_attn_simt(a, params->dtype, static_cast<cudaStream_t>(stream)), "decode launch");
+}
+
+}  // namespace
+
+extern "C" {
+
+g4_status g4_attn_decode(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers, int32_t layer,
+                         const void* q, const int32_t* seq_lens, int32_t B, int32_t max_seq_len, void* out,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_common(params, caches, n_layers, layer, q, nullptr, nullptr, nullptr, nullptr, false, seq_lens, B,
+                       max_seq_len, out, workspace, workspace_bytes, stream);
+}
+
+g4_status g4_decode_step(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers, int32_t layer,
+                         const void* q_in, const void* k_in, const void* v_in, const float* q_norm_w,
+                         const float* k_norm_w, const int32_t* seq_lens, int32_t B, int32_t max_seq_len, void* out,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_common(params, caches, n_layers, layer, q_in, k_in, v_in, q_norm_w, k_norm_w, true, seq_lens, B,
+                       max_seq_len, out, workspace, workspace_bytes, stream);
 }
 
 g4_status g4_attn_decode_noalloc(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
@@ -355,9 +409,19 @@ g4_status g4_attn_decode_noalloc(const g4_layer_params* params, const g4_kv_cach
   cudaError_t e = cudaSuccess;
   void* scratch = noalloc_scratch(&e);
   if (scratch == nullptr) return fail(G4_ERR_CUDA, "cannot resolve the built-in decode scratch: %s", cudaGetErrorString(e));
-  // Same kernels and split plan as g4_attn_decode; the split partials go to
-  // the built-in array.  Every partial a call's combine reads is written by
-  // that call's split kernel first, so nothing needs clearing between calls.
+  // Same kernels and split plan as g4_attn_decode, with the split partials in
+  // the built-in array.  The partials are written before they are read; the
+  // splits' arrival counters must start at zero, so they are cleared first.
+  if (B >= 1 && max_seq_len >= 1) {
+    const g4::DecodePlan plan = g4::decode_plan(params->layer_type == G4_SLIDING, params->window,
+                                                params->head_dim, params->n_heads, params->n_kv_heads, B,
+                                                max_seq_len);
+    if (plan.t_bytes > 0) {
+      e = cudaMemsetAsync(static_cast<uint8_t*>(scratch) + plan.o_bytes + 2 * plan.m_bytes, 0, plan.t_bytes,
+                          static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_status(e, "clearing the built-in decode scratch");
+    }
+  }
   return g4_attn_decode(params, caches, n_layers, layer, q, seq_lens, B, max_seq_len, out, scratch,
                         kNoAllocScratchBytes, stream);
 }

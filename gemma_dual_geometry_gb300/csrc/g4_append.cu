@@ -35,6 +35,8 @@ __global__ void __launch_bounds__(128) append_normrope_kernel(const __grid_const
   __shared__ float s_cos[HALF];
   __shared__ float s_sin[HALF];
 
+  pdl_wait();
+  pdl_trigger();
   const int tok = blockIdx.x;  // b * T + t
   const int b = tok / a.T;
   const int pos = a.positions[tok];
@@ -119,18 +121,31 @@ __global__ void __launch_bounds__(128) append_normrope_kernel(const __grid_const
   }
 }
 
+template <typename Kern>
+cudaError_t launch_pdl(Kern kern, dim3 grid, cudaStream_t s, const AppendArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(128);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
 template <typename T>
 cudaError_t launch_t(const AppendArgs& a, cudaStream_t s) {
   const int nrows = a.H + (a.k_in ? 2 * a.Hkv : 0);
   dim3 grid(a.B * a.T, (nrows + a.rows_per_cta - 1) / a.rows_per_cta);
   switch (a.hd) {
-    case 64: append_normrope_kernel<T, 64><<<grid, 128, 0, s>>>(a); break;
-    case 128: append_normrope_kernel<T, 128><<<grid, 128, 0, s>>>(a); break;
-    case 256: append_normrope_kernel<T, 256><<<grid, 128, 0, s>>>(a); break;
-    case 512: append_normrope_kernel<T, 512><<<grid, 128, 0, s>>>(a); break;
+    case 64: return launch_pdl(append_normrope_kernel<T, 64>, grid, s, a);
+    case 128: return launch_pdl(append_normrope_kernel<T, 128>, grid, s, a);
+    case 256: return launch_pdl(append_normrope_kernel<T, 256>, grid, s, a);
+    case 512: return launch_pdl(append_normrope_kernel<T, 512>, grid, s, a);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace

@@ -17,14 +17,24 @@
 //
 // Inside a warp, lane l owns HD/32 elements of every row (16-byte pieces
 // l, l+32, ... so shared-memory reads are conflict-free).  For a batch of
-// KB = min(16/G, 4 KB of rows) keys the lane forms KB*G partial dot products with packed f32x2
-// FMAs, a butterfly reduce-scatter turns the KB*G partials of 32 lanes into
-// KB*G full scores, the scores go through shared memory so every lane holds
-// all of them, and the online softmax (log2 domain; q is pre-scaled by
-// attn_scale*log2(e)) and the P.V update run redundantly per lane with no
-// further shuffles.  Warps merge their (m, l, o) at the end; with one split
-// the CTA writes the normalised output, otherwise an un-normalised partial
-// that launch_attn_combine merges with log-sum-exp weights.
+// KB = min(16/G, 4 KB of rows) keys the lane forms KB*G partial dot products
+// with packed f32x2 FMAs, a butterfly reduce-scatter turns the KB*G partials
+// of 32 lanes into KB*G full scores, the scores go through shared memory so
+// every lane holds all of them, and the online softmax (log2 domain; q is
+// pre-scaled by attn_scale*log2(e)) and the P.V update run redundantly per
+// lane with no further shuffles.  Warps merge their (m, l, o) through shared
+// memory.  With one split the CTA writes the normalised output; otherwise it
+// writes an un-normalised partial, takes a ticket from an atomic counter,
+// and the CTA that takes the last ticket of its (query row, kv head) merges
+// all partials with log-sum-exp weights and writes the output (no CTA ever
+// waits for another).
+//
+// The FUSED variant (decode step) starts from the new token's raw q / k / v:
+// every CTA norms and ropes its q heads itself, and the CTA whose split holds
+// position L-1 norms/ropes the new k and v (cortiq-engine `rms`, `rms_plain`,
+// rotate_half as in taconite `rope_half`), stores them into the cache row
+// L-1, and uses them as its last key -- the append and the attention of one
+// decode step in a single launch.
 #include <math.h>
 
 #include "g4_device.cuh"
@@ -33,10 +43,12 @@
 namespace g4 {
 namespace {
 
-constexpr int kNW = 4;   // warps per CTA
-constexpr int kNST = 3;  // stages per warp
-constexpr int kNPMax = 16;  // partial scores per reduce-scatter batch, at most
+constexpr int kNW = 4;            // warps per CTA
+constexpr int kNST = 3;           // stages per warp
+constexpr int kNPMax = 16;        // partial scores per reduce-scatter batch, at most
 constexpr int kStageMaxB = 4096;  // bytes of K (and of V) a reduce batch may span
+constexpr double kInv2Pi = 0.15915494309189533576888376337251;  // 1 / (2 pi)
+constexpr double k2Pi = 6.2831853071795864769252867665590;      // 2 pi
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
@@ -78,27 +90,115 @@ struct SimtCfg {
   static constexpr int RING_B = kNW * kNST * 2 * STAGE_B;
   static constexpr int MERGE_B = kNW * G * (HD + 2) * 4;
   static constexpr int AREA_B = RING_B > MERGE_B ? RING_B : MERGE_B;
-  static constexpr int SMEM_B = AREA_B + kNW * kNST * 8 + kNW * kNPMax * 4;
+  // after the area: barriers, per-warp score buffers, cos/sin table, merge weights, flag
+  static constexpr int BAR_OFF = AREA_B;
+  static constexpr int SC_OFF = BAR_OFF + kNW * kNST * 8;
+  static constexpr int COS_OFF = SC_OFF + kNW * kNPMax * 4;
+  static constexpr int W_OFF = COS_OFF + HD * 4;
+  static constexpr int FLAG_OFF = W_OFF + G * kMaxSplits * 4;
+  static constexpr int SMEM_B = FLAG_OFF + 16;
   static_assert(NP >= 2 && NP <= 16 && (NP & (NP - 1)) == 0, "reduce batch");
   static_assert(SMEM_B <= 232448, "shared memory budget");
 };
 
+// Lane l's elements of a row: pieces l + 32c (c < NPC) of PE elements.
+template <typename T, int NPC, int PE>
+__device__ __forceinline__ void load_row(const T* row, int lane, float* f) {
+#pragma unroll
+  for (int c = 0; c < NPC; ++c) load_elems<PE>(row + (lane + 32 * c) * PE, f + c * PE);
+}
+
+template <typename T, int NPC, int PE>
+__device__ __forceinline__ void store_row(T* row, int lane, const float* f) {
+#pragma unroll
+  for (int c = 0; c < NPC; ++c) store_elems<PE>(row + (lane + 32 * c) * PE, f + c * PE);
+}
+
+template <int N>
+__device__ __forceinline__ void to_f2(const float* f, float2 (&x)[N / 2]) {
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) x[i] = make_float2(f[2 * i], f[2 * i + 1]);
+}
+
 template <typename T, int NPC, int PE>
 __device__ __forceinline__ void load_row_f2(const T* row, int lane, float2 (&x)[NPC * PE / 2]) {
   float f[NPC * PE];
-#pragma unroll
-  for (int c = 0; c < NPC; ++c) load_elems<PE>(row + (lane + 32 * c) * PE, f + c * PE);
-#pragma unroll
-  for (int i = 0; i < NPC * PE / 2; ++i) x[i] = make_float2(f[2 * i], f[2 * i + 1]);
+  load_row<T, NPC, PE>(row, lane, f);
+  to_f2<NPC * PE>(f, x);
 }
 
-template <typename T, int HD, int G>
+// Round through the storage type (what a stored row would hold).
+template <typename T>
+__device__ __forceinline__ float through(float x) {
+  if constexpr (sizeof(T) == 2) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+  } else {
+    return x;
+  }
+}
+
+// RMSNorm (optional weight) then rotate_half RoPE of one row held in the lane
+// layout above; the partner of element d is d +- HD/2, which is the same lane
+// (NPC >= 2) or lane ^ 16 (NPC == 1).  Result rounded through T.
+template <typename T, int HD, int NPC, int PE>
+__device__ __forceinline__ void norm_rope_row(float* f, const float* w, bool rope, const float* s_cos,
+                                              const float* s_sin, int n_rot, float eps, int lane) {
+  constexpr int EL = NPC * PE;
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < EL; ++i) ss = fmaf(f[i], f[i], ss);
+  ss = warp_sum(ss);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(HD) + eps);
+  if (w != nullptr) {
+    float wf[EL];
+    load_row<float, NPC, PE>(w, lane, wf);
+#pragma unroll
+    for (int i = 0; i < EL; ++i) f[i] = f[i] * inv * wf[i];
+  } else {
+#pragma unroll
+    for (int i = 0; i < EL; ++i) f[i] *= inv;
+  }
+  if (rope) {
+    float fp[EL];
+    if constexpr (NPC >= 2) {
+#pragma unroll
+      for (int c = 0; c < NPC; ++c)
+#pragma unroll
+        for (int e = 0; e < PE; ++e) fp[c * PE + e] = f[((c + NPC / 2) % NPC) * PE + e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < PE; ++e) fp[e] = __shfl_xor_sync(0xffffffffu, f[e], 16);
+    }
+#pragma unroll
+    for (int c = 0; c < NPC; ++c) {
+#pragma unroll
+      for (int e = 0; e < PE; ++e) {
+        const int d = (lane + 32 * c) * PE + e;
+        const bool lower = d < HD / 2;
+        const int j = lower ? d : d - HD / 2;
+        if (j < n_rot) {
+          const float cs = s_cos[j], sn = s_sin[j];
+          const float x = f[c * PE + e], y = fp[c * PE + e];
+          f[c * PE + e] = lower ? (x * cs - y * sn) : (x * cs + y * sn);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < EL; ++i) f[i] = through<T>(f[i]);
+}
+
+template <typename T, int HD, int G, bool FUSED>
 __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_constant__ AttnSimtArgs a) {
   using C = SimtCfg<T, HD, G>;
   constexpr int EL2 = C::EL / 2;
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::AREA_B);
-  float* sc_all = reinterpret_cast<float*>(bars + kNW * kNST);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  float* sc_all = reinterpret_cast<float*>(smem + C::SC_OFF);
+  float* s_cos = reinterpret_cast<float*>(smem + C::COS_OFF);
+  float* s_sin = s_cos + HD / 2;
+  float* s_w = reinterpret_cast<float*>(smem + C::W_OFF);
+  int* s_flag = reinterpret_cast<int*>(smem + C::FLAG_OFF);
 
   const int split = blockIdx.x % a.nsplit;
   const int rest = blockIdx.x / a.nsplit;
@@ -108,6 +208,14 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
   const int t = bt % a.T;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  uint64_t* wbar = bars + warp * kNST;
+  if (lane == 0) {
+    for (int i = 0; i < kNST; ++i) mbar_init(smem_u32(&wbar[i]), 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  pdl_wait();
+  pdl_trigger();
 
   // Query position and visible key range [kbeg, L).
   int L;
@@ -119,19 +227,15 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
   const int kbeg = a.sliding ? max(0, L - a.window) : 0;
   const int k0 = kbeg + split * a.chunk;
   const int k1 = min(L, k0 + a.chunk);
-  const int nkeys = max(0, k1 - k0);
+  // FUSED: the CTA holding position L-1 computes that key itself.
+  const bool new_key = FUSED && a.k_raw != nullptr && (L - 1 >= k0) && (L - 1 < k1);
+  const int k1c = new_key ? L - 1 : k1;  // keys streamed from the cache
+  const int nkeys = max(0, k1c - k0);
   const int nstages = (nkeys + C::SK - 1) / C::SK;
 
   uint8_t* ring = smem + warp * (kNST * 2 * C::STAGE_B);
-  uint64_t* wbar = bars + warp * kNST;
   float* sc = sc_all + warp * kNPMax;
   bool aborted = false;
-
-  if (lane == 0) {
-    for (int i = 0; i < kNST; ++i) mbar_init(smem_u32(&wbar[i]), 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
 
   const size_t head_base = (static_cast<size_t>(b) * a.Hkv + kvh) * a.max_len;
   const T* gk = static_cast<const T*>(a.ck) + head_base * HD;
@@ -139,7 +243,7 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
 
   auto issue = [&](int st_idx, int buf) {
     const int kk0 = k0 + st_idx * C::SK;
-    const int n = min(C::SK, k1 - kk0);
+    const int n = min(C::SK, k1c - kk0);
     const uint32_t bytes = static_cast<uint32_t>(n) * C::ROWB;
     const uint32_t bar = smem_u32(&wbar[buf]);
     mbar_arrive_expect_tx(bar, 2 * bytes);
@@ -154,17 +258,33 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
     }
   }
 
+  if constexpr (FUSED) {
+    // cos/sin of the new token's position, angle reduced in float64
+    const int pos = L - 1;
+    for (int j = threadIdx.x; j < HD / 2; j += blockDim.x) {
+      float c = 1.0f, s = 0.0f;
+      if (j < a.n_rot) {
+        const double ang = static_cast<double>(pos) * static_cast<double>(a.inv_freq[j]);
+        const double k = rint(ang * kInv2Pi);
+        sincosf(static_cast<float>(fma(-k, k2Pi, ang)), &s, &c);
+      }
+      s_cos[j] = c;
+      s_sin[j] = s;
+    }
+    __syncthreads();
+  }
+
   // q of the G heads, pre-scaled into the log2 domain.
   float2 q2[G][EL2];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     const T* qrow = static_cast<const T*>(a.q) + (static_cast<size_t>(bt) * a.H + kvh * G + h) * HD;
-    load_row_f2<T, C::NPC, C::PE>(qrow, lane, q2[h]);
+    float f[C::EL];
+    load_row<T, C::NPC, C::PE>(qrow, lane, f);
+    if constexpr (FUSED) norm_rope_row<T, HD, C::NPC, C::PE>(f, a.q_w, true, s_cos, s_sin, a.n_rot, a.eps, lane);
 #pragma unroll
-    for (int i = 0; i < EL2; ++i) {
-      q2[h][i].x *= a.scale_log2;
-      q2[h][i].y *= a.scale_log2;
-    }
+    for (int i = 0; i < C::EL; ++i) f[i] *= a.scale_log2;
+    to_f2<C::EL>(f, q2[h]);
   }
 
   float m[G], l[G];
@@ -186,7 +306,7 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
       aborted = true;
       break;
     }
-    const int n = min(C::SK, k1 - (k0 + st_idx * C::SK));
+    const int n = min(C::SK, k1c - (k0 + st_idx * C::SK));
     const T* sk = reinterpret_cast<const T*>(ring + buf * 2 * C::STAGE_B);
     const T* sv = reinterpret_cast<const T*>(ring + buf * 2 * C::STAGE_B + C::STAGE_B);
 
@@ -270,6 +390,43 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
       warp_wait(smem_u32(&wbar[it % kNST]), (it / kNST) & 1, nullptr);
     }
   }
+
+  if constexpr (FUSED) {
+    if (new_key && warp == 0) {
+      // the new token's k and v: normed (+ roped for k), stored at row L-1, used as a key
+      const size_t row = (head_base + (L - 1)) * HD;
+      const size_t raw = (static_cast<size_t>(b) * a.Hkv + kvh) * HD;
+      float kf[C::EL], vf[C::EL];
+      load_row<T, C::NPC, C::PE>(static_cast<const T*>(a.k_raw) + raw, lane, kf);
+      load_row<T, C::NPC, C::PE>(static_cast<const T*>(a.v_raw) + raw, lane, vf);
+      norm_rope_row<T, HD, C::NPC, C::PE>(kf, a.k_w, true, s_cos, s_sin, a.n_rot, a.eps, lane);
+      norm_rope_row<T, HD, C::NPC, C::PE>(vf, nullptr, false, s_cos, s_sin, a.n_rot, a.eps, lane);
+      store_row<T, C::NPC, C::PE>(static_cast<T*>(a.cache_k) + row, lane, kf);
+      store_row<T, C::NPC, C::PE>(static_cast<T*>(a.cache_v) + row, lane, vf);
+      float2 kx[EL2], vx[EL2];
+      to_f2<C::EL>(kf, kx);
+      to_f2<C::EL>(vf, vx);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int i = 0; i < EL2; ++i) acc = __ffma2_rn(q2[h][i], kx[i], acc);
+        const float s = warp_sum(acc.x + acc.y);
+        const float m_new = fmaxf(m[h], s);
+        const float alpha = (m[h] == -INFINITY) ? 0.0f : exp2f(m[h] - m_new);
+        const float pn = exp2f(s - m_new);
+        l[h] = l[h] * alpha + pn;
+        m[h] = m_new;
+        const float2 pp = make_float2(pn, pn);
+#pragma unroll
+        for (int i = 0; i < EL2; ++i) {
+          o2[h][i].x *= alpha;
+          o2[h][i].y *= alpha;
+          o2[h][i] = __ffma2_rn(pp, vx[i], o2[h][i]);
+        }
+      }
+    }
+  }
   __syncthreads();
 
   // Merge the warps' (m, l, o) through shared memory (the ring is free now).
@@ -331,47 +488,83 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
       }
     }
   }
-}
+  if (a.nsplit == 1) return;
 
-// Log-sum-exp merge of the split partials of one (query row, head).
-template <typename T, int HD>
-__global__ void __launch_bounds__(128) attn_combine_kernel(const __grid_constant__ AttnSimtArgs a) {
-  const int head = blockIdx.x;
-  const int bt = blockIdx.y;
-  const size_t p0 = (static_cast<size_t>(bt) * a.H + head) * a.nsplit;
-  float M = -INFINITY;
-  for (int s = 0; s < a.nsplit; ++s) M = fmaxf(M, a.ws_m[p0 + s]);
-  float Ls = 0.0f;
-  for (int s = 0; s < a.nsplit; ++s) {
-    const float ms = a.ws_m[p0 + s];
-    if (ms != -INFINITY) Ls += exp2f(ms - M) * a.ws_l[p0 + s];
-  }
-  const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
-  T* dst = static_cast<T*>(a.out) + (static_cast<size_t>(bt) * a.H + head) * HD;
-  for (int d = threadIdx.x; d < HD; d += blockDim.x) {
-    float O = 0.0f;
-    for (int s = 0; s < a.nsplit; ++s) {
-      const float ms = a.ws_m[p0 + s];
-      if (ms != -INFINITY) O += exp2f(ms - M) * a.ws_o[(p0 + s) * HD + d];
+  // Ticket: the CTA that completes the set of splits of this (row, kv head)
+  // merges them.  Writers publish their partial before taking a ticket.
+  __threadfence();
+  __syncthreads();
+  unsigned* ticket = a.tickets + static_cast<size_t>(bt) * a.Hkv + kvh;
+  if (threadIdx.x == 0) *s_flag = (atomicAdd(ticket, 1u) == static_cast<unsigned>(a.nsplit - 1)) ? 1 : 0;
+  __syncthreads();
+  if (*s_flag == 0) return;
+  __threadfence();
+  for (int h = warp; h < G; h += kNW) {
+    const size_t p0 = (static_cast<size_t>(bt) * a.H + kvh * G + h) * a.nsplit;
+    float M = -INFINITY;
+    for (int s = lane; s < a.nsplit; s += 32) M = fmaxf(M, __ldcg(a.ws_m + p0 + s));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    float Ls = 0.0f;
+    for (int s = lane; s < a.nsplit; s += 32) {
+      const float ms_ = __ldcg(a.ws_m + p0 + s);
+      const float w = (ms_ == -INFINITY) ? 0.0f : exp2f(ms_ - M);
+      s_w[h * kMaxSplits + s] = w;
+      Ls += w * __ldcg(a.ws_l + p0 + s);
     }
-    const float val = O * inv;
-    store_elems<1>(dst + d, &val);
+    Ls = warp_sum(Ls);
+    const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+    __syncwarp();
+    for (int s = lane; s < a.nsplit; s += 32) s_w[h * kMaxSplits + s] *= inv;
   }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * HD; idx += blockDim.x) {
+    const int h = idx / HD;
+    const int d = idx % HD;
+    const size_t p0 = (static_cast<size_t>(bt) * a.H + kvh * G + h) * a.nsplit;
+    const float* wr = s_w + h * kMaxSplits;
+    float O = 0.0f;
+#pragma unroll 4
+    for (int s = 0; s < a.nsplit; ++s) O = fmaf(wr[s], __ldcg(a.ws_o + (p0 + s) * HD + d), O);
+    T* dst = static_cast<T*>(a.out) + (static_cast<size_t>(bt) * a.H + kvh * G + h) * HD + d;
+    store_elems<1>(dst, &O);
+  }
+  if (threadIdx.x == 0) *ticket = 0u;  // ready for the next call
 }
 
-template <typename T, int HD, int G>
-cudaError_t launch_simt_hg(const AttnSimtArgs& a, cudaStream_t s) {
+template <typename Kern>
+cudaError_t launch_pdl(Kern kern, unsigned grid, unsigned block, size_t smem, cudaStream_t s,
+                       const AttnSimtArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+template <typename T, int HD, int G, bool FUSED>
+cudaError_t launch_simt_hgf(const AttnSimtArgs& a, cudaStream_t s) {
   using C = SimtCfg<T, HD, G>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, HD, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::SMEM_B);
+    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, HD, G, FUSED>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_B);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const long long nblk = static_cast<long long>(a.nsplit) * a.Hkv * a.B * a.T;
-  attn_simt_kernel<T, HD, G><<<static_cast<unsigned>(nblk), kNW * 32, C::SMEM_B, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(attn_simt_kernel<T, HD, G, FUSED>, static_cast<unsigned>(nblk), kNW * 32, C::SMEM_B, s, a);
+}
+
+template <typename T, int HD, int G>
+cudaError_t launch_simt_hg(const AttnSimtArgs& a, cudaStream_t s) {
+  return a.fused ? launch_simt_hgf<T, HD, G, true>(a, s) : launch_simt_hgf<T, HD, G, false>(a, s);
 }
 
 template <typename T, int HD>
@@ -399,50 +592,35 @@ cudaError_t launch_simt_t(const AttnSimtArgs& a, cudaStream_t s) {
   }
 }
 
-template <typename T>
-cudaError_t launch_combine_t(const AttnSimtArgs& a, cudaStream_t s) {
-  dim3 grid(a.H, a.B * a.T);
-  switch (a.hd) {
-    case 64: attn_combine_kernel<T, 64><<<grid, 128, 0, s>>>(a); break;
-    case 128: attn_combine_kernel<T, 128><<<grid, 128, 0, s>>>(a); break;
-    case 256: attn_combine_kernel<T, 256><<<grid, 128, 0, s>>>(a); break;
-    case 512: attn_combine_kernel<T, 512><<<grid, 128, 0, s>>>(a); break;
-    default: return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 cudaError_t launch_attn_simt(const AttnSimtArgs& a, int dtype, cudaStream_t s) {
   return dtype == 1 ? launch_simt_t<__nv_bfloat16>(a, s) : launch_simt_t<float>(a, s);
 }
 
-cudaError_t launch_attn_combine(const AttnSimtArgs& a, int dtype, cudaStream_t s) {
-  return dtype == 1 ? launch_combine_t<__nv_bfloat16>(a, s) : launch_combine_t<float>(a, s);
-}
-
 DecodePlan decode_plan(int sliding, int window, int hd, int H, int Hkv, int B, int max_seq_len) {
   DecodePlan p;
   const int span = sliding ? (max_seq_len < window ? max_seq_len : window) : max_seq_len;
   const int units = B * Hkv;
-  const int target_ctas = 1216;  // eight CTAs per SM on a 152-SM GPU
+  const int target_ctas = 608;  // four CTAs per SM on a 152-SM GPU
   int nsplit = (target_ctas + units - 1) / units;
-  const int by_len = (span + 255) / 256;  // at least 256 keys per split
+  const int by_len = (span + 63) / 64;  // at least 64 keys per split
   if (nsplit > by_len) nsplit = by_len;
+  if (nsplit > kMaxSplits) nsplit = kMaxSplits;
   if (nsplit < 1) nsplit = 1;
   int chunk = (span + nsplit - 1) / nsplit;
-  chunk = (chunk + 63) / 64 * 64;
+  chunk = (chunk + 15) / 16 * 16;
   nsplit = (span + chunk - 1) / chunk;
   p.chunk = chunk;
   p.nsplit = nsplit;
   if (nsplit <= 1) {
-    p.ws_bytes = 0;
+    p.o_bytes = p.m_bytes = p.t_bytes = p.ws_bytes = 0;
   } else {
     const size_t np = static_cast<size_t>(B) * H * nsplit;
-    const size_t o_b = (np * hd * 4 + 255) / 256 * 256;
-    const size_t m_b = (np * 4 + 255) / 256 * 256;
-    p.ws_bytes = o_b + 2 * m_b;
+    p.o_bytes = (np * hd * 4 + 255) / 256 * 256;
+    p.m_bytes = (np * 4 + 255) / 256 * 256;
+    p.t_bytes = (static_cast<size_t>(B) * Hkv * 4 + 255) / 256 * 256;
+    p.ws_bytes = p.o_bytes + 2 * p.m_bytes + p.t_bytes;
   }
   return p;
 }

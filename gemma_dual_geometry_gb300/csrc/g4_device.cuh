@@ -124,6 +124,15 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Kernels launched with programmatic stream serialisation may start while the
+// previous kernel on the stream is finishing.  pdl_wait() blocks until that
+// kernel has completed and its memory is visible; every kernel calls it
+// before its first global-memory access.  pdl_trigger() lets the next kernel
+// start launching.  Both are no-ops for a normal launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {

@@ -32,8 +32,13 @@ cudaError_t launch_append(const AppendArgs& a, int dtype, cudaStream_t s);
 // Steps a5 (float32) and a6: split-KV softmax attention on CUDA cores.
 // mode 0 (decode): one query per sequence at position base[b] - 1, keys
 //   [kstart, base[b]); mode 1 (prefill): query t at position base[b] + t.
+// With fused set (decode only), q / k_raw / v_raw are the new token's raw
+// projections: each CTA norms and ropes its q heads, and the CTA whose split
+// holds position L-1 norms/ropes the new k and v, writes them to the cache
+// row L-1 and uses them as the last key (the append of step a4 in the same
+// launch).
 struct AttnSimtArgs {
-  const void* q;    // [B][T][H][hd]
+  const void* q;    // [B][T][H][hd] (raw when fused)
   const void* ck;   // [B][Hkv][max_len][hd]
   const void* cv;
   void* out;        // [B][T][H][hd]
@@ -41,6 +46,7 @@ struct AttnSimtArgs {
   float* ws_o;      // [B*T][H][nsplit][hd] partial outputs (nsplit > 1)
   float* ws_m;      // [B*T][H][nsplit] running max (log2 domain)
   float* ws_l;      // [B*T][H][nsplit] softmax denominators
+  unsigned* tickets;  // [B*T][Hkv] arrival counters of the splits (zero between calls)
   int* err;
   int mode;
   int B, T, H, Hkv, hd, max_len;
@@ -49,9 +55,19 @@ struct AttnSimtArgs {
   int chunk;        // keys per split
   int nsplit;
   float scale_log2;  // attn_scale * log2(e)
+  // fused append of the new token
+  int fused;
+  const void* k_raw;  // [B][Hkv][hd], null on a shared layer
+  const void* v_raw;
+  const float* q_w;
+  const float* k_w;
+  void* cache_k;      // the layer's own cache (written at row L-1)
+  void* cache_v;
+  float eps;
+  int n_rot;
+  float inv_freq[kMaxHalf];
 };
 cudaError_t launch_attn_simt(const AttnSimtArgs& a, int dtype, cudaStream_t s);
-cudaError_t launch_attn_combine(const AttnSimtArgs& a, int dtype, cudaStream_t s);
 
 // Step a5 (bf16): tcgen05 flash prefill.
 struct PrefillTcArgs {
@@ -68,9 +84,12 @@ struct PrefillTcArgs {
 cudaError_t launch_prefill_tc(const PrefillTcArgs& a, cudaStream_t s);
 
 // Decode split plan shared by the workspace query and the launch.
+// Workspace layout: ws_o, then ws_m, ws_l, tickets, each 256-byte aligned.
+constexpr int kMaxSplits = 128;
 struct DecodePlan {
   int chunk;
   int nsplit;
+  size_t o_bytes, m_bytes, t_bytes;  // sizes of the four regions (ws_m and ws_l share m_bytes)
   size_t ws_bytes;
 };
 DecodePlan decode_plan(int sliding, int window, int hd, int H, int Hkv, int B, int max_seq_len);

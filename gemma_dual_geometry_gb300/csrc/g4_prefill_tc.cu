@@ -85,6 +85,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  pdl_wait();
+  pdl_trigger();
 
   // Block -> (q tile, sequence, head, output half); heaviest (last) tiles first.
   const int nqt = (a.T + kBM - 1) / kBM;
@@ -474,8 +476,17 @@ cudaError_t launch_hd(const PrefillTcArgs& a, cudaStream_t s) {
   }
   const int nqt = (a.T + kBM - 1) / kBM;
   const long long nblk = static_cast<long long>(nqt) * a.H * a.B * C::NDH;
-  prefill_tc_kernel<HD><<<static_cast<unsigned>(nblk), kThreads, C::SMEM_B, s>>>(mq, mk, mv, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(nblk));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::SMEM_B;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD>, mq, mk, mv, a);
 }
 
 }  // namespace

@@ -52,6 +52,9 @@ SIGNATURES = {
     "g4_attn_decode_workspace_size": (ctypes.c_size_t, [_P(G4LayerParams), _i32, _i32]),
     "g4_attn_decode": (_i32, [_P(G4LayerParams), _P(G4KVCache), _i32, _i32, _c_void_p, _c_void_p, _i32, _i32,
                               _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p]),
+    "g4_decode_step": (_i32, [_P(G4LayerParams), _P(G4KVCache), _i32, _i32, _c_void_p, _c_void_p, _c_void_p,
+                              _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _c_void_p, ctypes.c_size_t,
+                              _c_void_p]),
     "g4_attn_decode_noalloc": (_i32, [_P(G4LayerParams), _P(G4KVCache), _i32, _i32, _c_void_p, _c_void_p, _i32,
                                       _i32, _c_void_p, _c_void_p]),
     "g4_last_error": (ctypes.c_char_p, []),
@@ -148,7 +151,14 @@ def g4_attn_decode(params, caches, layer, q, seq_lens, B, max_seq_len, out, work
                                 max_seq_len, _ptr(out), _ptr(workspace), int(workspace_bytes), _stream(stream, q)))
 
 
-G4_NOALLOC_SCRATCH_BYTES = 16 << 20
+def g4_decode_step(params, caches, layer, q_in, k_in, v_in, q_norm_w, k_norm_w, seq_lens, B, max_seq_len, out,
+                   workspace=None, workspace_bytes=0, stream=None):
+    _check(lib().g4_decode_step(ctypes.byref(params), caches, len(caches), layer, _ptr(q_in), _ptr(k_in), _ptr(v_in),
+                                _ptr(q_norm_w), _ptr(k_norm_w), _ptr(seq_lens), B, max_seq_len, _ptr(out),
+                                _ptr(workspace), int(workspace_bytes), _stream(stream, q_in)))
+
+
+G4_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 def g4_attn_decode_noalloc(params, caches, layer, q, seq_lens, B, max_seq_len, out, stream=None):

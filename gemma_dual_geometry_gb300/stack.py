@@ -45,7 +45,7 @@ class AttnStack:
         self.ws = {}
         for l, p in enumerate(self.params):
             nb = G.g4_attn_decode_workspace_size(p, self.B, Lmax)
-            self.ws[l] = (torch.empty(max(nb, 16), dtype=torch.uint8, device=self.device), nb)
+            self.ws[l] = (torch.zeros(max(nb, 16), dtype=torch.uint8, device=self.device), nb)
 
     def owns(self, l):
         return self.src[l] < 0
@@ -65,6 +65,12 @@ class AttnStack:
         G.g4_attn_decode(self.params[l], self.table, l, q_out, seq_lens, self.B, max_seq_len, out, ws, nb,
                          stream=stream)
 
+    def decode_step(self, l, q, k, v, qw, kw, seq_lens, max_seq_len, out, stream=None):
+        """Fused append of the new token + decode attention (one launch)."""
+        ws, nb = self.ws[l]
+        G.g4_decode_step(self.params[l], self.table, l, q, k, v, qw, kw, seq_lens, self.B, max_seq_len, out, ws, nb,
+                         stream=stream)
+
     def decode_launches(self, l):
-        """Kernels one g4_attn_decode call launches (split kernel, plus the combine when split)."""
-        return 2 if self.ws[l][1] > 0 else 1
+        """Kernels one g4_attn_decode or g4_decode_step call launches."""
+        return 1

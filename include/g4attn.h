@@ -171,8 +171,8 @@ g4_status g4_attn_prefill(const g4_layer_params* params, const g4_kv_cache* cach
                           void* out, void* stream);
 
 /*
- * Workspace bytes g4_attn_decode needs for this layer, batch and bound on the
- * sequence lengths (0 means no workspace is needed).
+ * Workspace bytes g4_attn_decode / g4_decode_step need for this layer, batch
+ * and bound on the sequence lengths (0 means no workspace is needed).
  */
 size_t g4_attn_decode_workspace_size(const g4_layer_params* params, int32_t B, int32_t max_seq_len);
 
@@ -187,21 +187,39 @@ size_t g4_attn_decode_workspace_size(const g4_layer_params* params, int32_t B, i
  *   out          [B][n_heads][head_dim]
  *   workspace    device scratch of at least g4_attn_decode_workspace_size()
  *                bytes (may be NULL when that is 0); caller-owned, 16-byte
- *                aligned, contents need no initialisation.
+ *                aligned.  Zero-fill it once before its first use: it holds
+ *                arrival counters that every call leaves at zero again.
  * Sliding layers read keys [max(0, L - window), L), full layers [0, L).  The
- * key range is split across CTAs (split-KV) and merged with a log-sum-exp
- * combine kernel.  Calls sharing a workspace must not overlap on the GPU.
+ * key range is split across CTAs (split-KV); the CTA that finishes last for a
+ * (sequence, kv head) merges the splits with log-sum-exp weights.  Calls
+ * sharing a workspace must not overlap on the GPU.
  */
 g4_status g4_attn_decode(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
                          int32_t layer, const void* q, const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
                          void* out, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Steps a4 + a6 (+ a7) in one launch: the decode step of one layer from the
+ * new token's raw projections.  Same result as g4_kv_append_normrope with
+ * positions[b] = seq_lens[b] - 1 (T = 1) followed by g4_attn_decode on its
+ * q_out, without the q_out round trip through memory:
+ *   q_in         [B][n_heads][head_dim] raw q of the new token
+ *   k_in, v_in   [B][n_kv_heads][head_dim] raw k / v (NULL on a shared layer)
+ *   q_norm_w, k_norm_w  float32 [head_dim] (k_norm_w NULL on a shared layer)
+ * On a layer that owns its cache the new k / v rows are written to row
+ * seq_lens[b] - 1 of caches[layer].  Other arguments as g4_attn_decode.
+ */
+g4_status g4_decode_step(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers, int32_t layer,
+                         const void* q_in, const void* k_in, const void* v_in, const float* q_norm_w,
+                         const float* k_norm_w, const int32_t* seq_lens, int32_t B, int32_t max_seq_len, void* out,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Bytes of device scratch built into the library for g4_attn_decode_noalloc
- * (16 MiB).  Every GPU that loads the library holds this array until the
+ * (8 MiB).  Every GPU that loads the library holds this array until the
  * process exits.
  */
-#define G4_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+#define G4_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 
 /*
  * g4_attn_decode without a workspace argument, for callers that cannot
@@ -220,8 +238,10 @@ g4_status g4_attn_decode(const g4_layer_params* params, const g4_kv_cache* cache
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  All calls share the one array and it keeps the last call's
- * contents: calls whose kernels overlap on the GPU (different streams, or
- * several threads) race on it and must be serialised by the caller.
+ * contents; each call first clears the part that must start at zero (the
+ * splits' arrival counters, an asynchronous memset on `stream`).  Calls
+ * whose kernels overlap on the GPU (different streams, or several threads)
+ * race on the array and must be serialised by the caller.
  */
 g4_status g4_attn_decode_noalloc(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
                                  int32_t layer, const void* q, const int32_t* seq_lens, int32_t B,

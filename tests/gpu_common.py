@@ -175,10 +175,11 @@ class LayerRun:
         return self
 
 
-def run_decode(geo, lens, Lmax, seed, max_seq_len=None, decode_fn=None):
+def run_decode(geo, lens, Lmax, seed, max_seq_len=None, fused=False, return_cache=False):
     """Cache rows [0, L-1) prefilled with N(0,1), the new token appended at
-    L-1, rows >= L NaN; then decode through the C ABI.
-    Returns (gpu_out, oracle_out, workspace_bytes)."""
+    L-1, rows >= L NaN; then decode through the C ABI -- append + decode, or
+    the fused decode step.  Returns (gpu_out, oracle_out, workspace_bytes)
+    (+ (gpu k cache, gpu v cache, oracle k, oracle v) with return_cache)."""
     B = len(lens)
     hd, H, Hkv, dt = geo["head_dim"], geo["n_heads"], geo["n_kv_heads"], geo["dtype"]
     lens = np.asarray(lens, dtype=np.int64)
@@ -194,16 +195,20 @@ def run_decode(geo, lens, Lmax, seed, max_seq_len=None, decode_fn=None):
     G.set_cache(table, 0, ck, cv, geo["layer_type"], hd, Hkv, Lmax, B, dt)
     p = params_of(geo)
     q = x["q"].to(DEV)
-    q_out = torch.empty_like(q)
-    pos = torch.tensor(lens - 1, dtype=torch.int32, device=DEV).view(B, 1)
-    G.g4_kv_append_normrope(p, table, 0, q, x["k"].to(DEV), x["v"].to(DEV), x["qw"].to(DEV), x["kw"].to(DEV), pos,
-                            B, 1, q_out)
     msl = int(max_seq_len or lens.max())
     wsb = G.g4_attn_decode_workspace_size(p, B, msl)
-    ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=DEV)
     out = torch.empty((B, H, hd), dtype=W.torch_dtype(dt), device=DEV)
     sl = torch.tensor(lens, dtype=torch.int32, device=DEV)
-    G.g4_attn_decode(p, table, 0, q_out.view(B, H, hd), sl, B, msl, out, ws, wsb)
+    if fused:
+        G.g4_decode_step(p, table, 0, q.view(B, H, hd), x["k"].to(DEV).view(B, Hkv, hd),
+                         x["v"].to(DEV).view(B, Hkv, hd), x["qw"].to(DEV), x["kw"].to(DEV), sl, B, msl, out, ws, wsb)
+    else:
+        q_out = torch.empty_like(q)
+        pos = torch.tensor(lens - 1, dtype=torch.int32, device=DEV).view(B, 1)
+        G.g4_kv_append_normrope(p, table, 0, q, x["k"].to(DEV), x["v"].to(DEV), x["qw"].to(DEV), x["kw"].to(DEV),
+                                pos, B, 1, q_out)
+        G.g4_attn_decode(p, table, 0, q_out.view(B, H, hd), sl, B, msl, out, ws, wsb)
     torch.cuda.synchronize()
     # oracle: same prefilled rows, its own append of the new token
     lp = oracle_lp(geo)
@@ -211,4 +216,6 @@ def run_decode(geo, lens, Lmax, seed, max_seq_len=None, decode_fn=None):
     oq = O.kv_append_normrope(lp, f64(x["q"]), f64(x["k"]), f64(x["v"]), f64(x["qw"]), f64(x["kw"]),
                               (lens - 1)[:, None], ok, ov)
     ref = O.attention(oq, ok, ov, (lens - 1)[:, None], lens, Hkv, geo["layer_type"], geo["window"], 1.0)
+    if return_cache:
+        return f64(out), ref[:, 0], wsb, (ck, cv, ok, ov)
     return f64(out), ref[:, 0], wsb

@@ -160,8 +160,22 @@ def test_decode_validation_and_workspace(L):
     assert dec(B=65) == G.G4_ERR_CAPACITY
     assert dec(B=0) == G.G4_OK
     # a sliding layer whose window is no longer than the minimum split needs no workspace
-    assert G.g4_attn_decode_workspace_size(_params(window=128), 64, 8192) == 0
+    assert G.g4_attn_decode_workspace_size(_params(window=64), 64, 8192) == 0    # one 64-key split
     assert L.g4_attn_decode_workspace_size(None, 64, 8192) == 0
+
+
+def test_decode_step_validation(L):
+    tab = _table([(G.G4_SLIDING, 256, 2, 100, 4, G.G4_BF16), None])
+
+    def st(p, layer, k, v, kw, qw=FAKE, B=4):
+        return _status(G.g4_decode_step, p, tab, layer, FAKE, k, v, qw, kw, FAKE, B, 100, FAKE, FAKE, 1 << 20, 0)
+
+    assert st(_params(), 0, None, FAKE, FAKE) == G.G4_ERR_INVALID_ARG           # owner needs k/v/k_norm_w
+    assert st(_params(), 0, FAKE, FAKE, FAKE, qw=None) == G.G4_ERR_INVALID_ARG  # q_norm_w required
+    assert st(_params(kv_share_src=0), 1, FAKE, None, None) == G.G4_ERR_INVALID_ARG  # shared: no k/v
+    assert st(_params(kv_share_src=0), 1, None, None, None, B=0) == G.G4_OK
+    assert st(_params(), 0, FAKE, FAKE, FAKE, B=5) == G.G4_ERR_CAPACITY
+    assert st(_params(head_dim=512), 0, FAKE, FAKE, FAKE) == G.G4_ERR_SHARE_MISMATCH
 
 
 def test_tiny_config_literal_layer_types_are_rejected(L):

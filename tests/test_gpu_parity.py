@@ -235,3 +235,50 @@ def test_decode_split_and_single_split_agree_with_oracle():
     assert w1 == 0 and w2 > 0
     assert_attn_close(g1, ref, W.BF16, "one split")
     assert_attn_close(g2, ref2, W.BF16, "many splits")
+
+
+# ---------------------------------------------------------------- a4 + a6 fused decode step
+
+@pytest.mark.parametrize("dtype,lt,hd,window,Hkv,lens", DECODE_CASES)
+def test_decode_step_parity_and_appended_rows(dtype, lt, hd, window, Hkv, lens):
+    geo = geometry(lt, hd, H=4 * Hkv, Hkv=Hkv, window=window, dtype=dtype)
+    Lmax = max(lens) + 8
+    gpu, ref, _, (ck, cv, ok, ov) = run_decode(geo, lens, Lmax, seed=700 + hd, fused=True, return_cache=True)
+    assert_attn_close(gpu, ref, dtype, "decode step")
+    # the new rows were written at L-1 (1 ulp of the oracle's append); rows >= L are untouched NaN
+    for b, L in enumerate(lens):
+        assert_stored_close(f64(ck[b, :, L - 1]), ok[b, :, L - 1], dtype, "new k row")
+        assert_stored_close(f64(cv[b, :, L - 1]), ov[b, :, L - 1], dtype, "new v row")
+        assert torch.isnan(ck[b, :, L:]).all() and torch.isnan(cv[b, :, L:]).all()
+
+
+def test_decode_step_shared_layer_and_gqa_groups():
+    # group 8 and group 1; and a shared layer reading the source cache
+    for H, Hkv, hd in ((16, 2, 64), (2, 2, 512)):
+        geo = geometry(F, hd, H=H, Hkv=Hkv)
+        gpu, ref, _ = run_decode(geo, [1, 333, 1025], 1100, seed=H + hd + 1, fused=True)
+        assert_attn_close(gpu, ref, W.BF16, f"decode step H={H} Hkv={Hkv}")
+    geo = geometry(S, 256, window=300)
+    B, Hkv, H, hd, Lmax = 3, 2, 8, 256, 700
+    lens = np.array([1, 299, 650])
+    ck = W.normal((B, Hkv, Lmax, hd), 81, W.BF16).to(DEV)
+    cv = W.normal((B, Hkv, Lmax, hd), 82, W.BF16).to(DEV)
+    table = G.cache_table(2)
+    G.set_cache(table, 0, ck, cv, S, hd, Hkv, Lmax, B, W.BF16)
+    q = W.normal((B, H, hd), 83, W.BF16).to(DEV)
+    qw = W.norm_weight(hd, 84).to(DEV)
+    sl = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    p1 = params_of(geo, src=0)
+    wsb = G.g4_attn_decode_workspace_size(p1, B, Lmax)
+    ws = torch.zeros(max(wsb, 16), dtype=torch.uint8, device=DEV)
+    before = ck.clone()
+    o_step = torch.empty_like(q)
+    G.g4_decode_step(p1, table, 1, q, None, None, qw, None, sl, B, Lmax, o_step, ws, wsb)
+    q_out = torch.empty_like(q)
+    G.g4_kv_append_normrope(p1, table, 1, q.view(B, 1, H, hd), None, None, qw, None, (sl - 1).view(B, 1), B, 1,
+                            q_out.view(B, 1, H, hd))
+    o_ref = torch.empty_like(q)
+    G.g4_attn_decode(p1, table, 1, q_out, sl, B, Lmax, o_ref, ws, wsb)
+    torch.cuda.synchronize()
+    assert torch.equal(before.view(torch.int16), ck.view(torch.int16))    # a shared layer writes nothing
+    assert_attn_close(f64(o_step), f64(o_ref), W.BF16, "shared-layer decode step vs append + decode")
