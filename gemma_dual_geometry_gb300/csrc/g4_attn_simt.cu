@@ -518,16 +518,54 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
     for (int s = lane; s < a.nsplit; s += 32) s_w[h * kMaxSplits + s] *= inv;
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < G * HD; idx += blockDim.x) {
-    const int h = idx / HD;
-    const int d = idx % HD;
-    const size_t p0 = (static_cast<size_t>(bt) * a.H + kvh * G + h) * a.nsplit;
-    const float* wr = s_w + h * kMaxSplits;
-    float O = 0.0f;
-#pragma unroll 4
-    for (int s = 0; s < a.nsplit; ++s) O = fmaf(wr[s], __ldcg(a.ws_o + (p0 + s) * HD + d), O);
-    T* dst = static_cast<T*>(a.out) + (static_cast<size_t>(bt) * a.H + kvh * G + h) * HD + d;
-    store_elems<1>(dst, &O);
+  // Each thread owns float4 groups of the G*HD outputs and keeps many loads in
+  // flight: 8 splits x up to 4 groups per round.
+  constexpr int NG4 = G * HD / 4;                        // float4 groups
+  constexpr int PER = (NG4 + kNW * 32 - 1) / (kNW * 32);  // groups per thread
+  float4 acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  const size_t pbase = (static_cast<size_t>(bt) * a.H + kvh * G) * a.nsplit;
+  for (int s0 = 0; s0 < a.nsplit; s0 += 8) {
+    float4 v[PER][8];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int g4i = threadIdx.x + i * kNW * 32;
+      const int h = (g4i * 4) / HD;
+      const int d = (g4i * 4) % HD;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int sp = s0 + u;
+        v[i][u] = (g4i < NG4 && sp < a.nsplit)
+                      ? __ldcg(reinterpret_cast<const float4*>(a.ws_o + ((pbase + static_cast<size_t>(h) * a.nsplit +
+                                                                           sp) * HD + d)))
+                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int g4i = threadIdx.x + i * kNW * 32;
+      const int h = g4i < NG4 ? (g4i * 4) / HD : 0;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float w = (s0 + u < a.nsplit) ? s_w[h * kMaxSplits + s0 + u] : 0.0f;
+        acc[i].x = fmaf(w, v[i][u].x, acc[i].x);
+        acc[i].y = fmaf(w, v[i][u].y, acc[i].y);
+        acc[i].z = fmaf(w, v[i][u].z, acc[i].z);
+        acc[i].w = fmaf(w, v[i][u].w, acc[i].w);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int g4i = threadIdx.x + i * kNW * 32;
+    if (g4i < NG4) {
+      const int h = (g4i * 4) / HD;
+      const int d = (g4i * 4) % HD;
+      T* dst = static_cast<T*>(a.out) + (static_cast<size_t>(bt) * a.H + kvh * G + h) * HD + d;
+      const float f[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
+      store_elems<4>(dst, f);
+    }
   }
   if (threadIdx.x == 0) *ticket = 0u;  // ready for the next call
 }
@@ -602,10 +640,17 @@ DecodePlan decode_plan(int sliding, int window, int hd, int H, int Hkv, int B, i
   DecodePlan p;
   const int span = sliding ? (max_seq_len < window ? max_seq_len : window) : max_seq_len;
   const int units = B * Hkv;
-  const int target_ctas = 608;  // four CTAs per SM on a 152-SM GPU
+  // Enough CTAs to keep every SM streaming (eight per SM of a 152-SM GPU),
+  // at least 64 keys per split, and at most sqrt(span / 8) splits so that the
+  // final merge (nsplit partials of G*hd floats) stays small next to the
+  // keys each split streams.
+  const int target_ctas = 1216;
   int nsplit = (target_ctas + units - 1) / units;
-  const int by_len = (span + 63) / 64;  // at least 64 keys per split
+  const int by_len = (span + 63) / 64;
+  int by_merge = static_cast<int>(sqrt(static_cast<double>(span) / 8.0));
+  if (by_merge < 4) by_merge = 4;
   if (nsplit > by_len) nsplit = by_len;
+  if (nsplit > by_merge) nsplit = by_merge;
   if (nsplit > kMaxSplits) nsplit = kMaxSplits;
   if (nsplit < 1) nsplit = 1;
   int chunk = (span + nsplit - 1) / nsplit;
