@@ -36,6 +36,7 @@
 // L-1, and uses them as its last key -- the append and the attention of one
 // decode step in a single launch.
 #include <math.h>
+#include <string.h>
 
 #include "g4_device.cuh"
 #include "g4_internal.h"
@@ -44,13 +45,31 @@ namespace g4 {
 namespace {
 
 constexpr int kNW = 4;            // warps per CTA
-constexpr int kNST = 3;           // stages per warp
 constexpr int kNPMax = 16;        // partial scores per reduce-scatter batch, at most
 constexpr int kStageMaxB = 4096;  // bytes of K (and of V) a reduce batch may span
 constexpr double kInv2Pi = 0.15915494309189533576888376337251;  // 1 / (2 pi)
 constexpr double k2Pi = 6.2831853071795864769252867665590;      // 2 pi
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+// d = a * b + c on two packed floats (one f32x2 instruction).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  unsigned long long ua, ub, uc, ud;
+  memcpy(&ua, &a, 8);
+  memcpy(&ub, &b, 8);
+  memcpy(&uc, &c, 8);
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(ud) : "l"(ua), "l"(ub), "l"(uc));
+  float2 d;
+  memcpy(&d, &ud, 8);
+  return d;
+}
+
+// 2^x with the hardware approximation (inputs here are <= 0; -inf gives 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // Sum of v[i] over the 32 lanes, scattered: lane l returns the total of index
 // l >> (5 - log2(NP)).  NP is a power of two in [2, 32].
@@ -87,13 +106,18 @@ struct SimtCfg {
   static constexpr int NB = (KB * ROWB >= 2048) ? 1 : 2048 / (KB * ROWB);  // batches per stage
   static constexpr int SK = KB * NB;                 // keys per stage
   static constexpr int STAGE_B = SK * ROWB;          // bytes of K (and of V) per stage
-  static constexpr int RING_B = kNW * kNST * 2 * STAGE_B;
+  // G*HD = 2048 needs ~180 registers for q and o alone: two CTAs per SM with
+  // three stages per warp; narrower heads fit three CTAs with two stages.
+  static constexpr int NST = (G * HD >= 2048) ? 3 : 2;   // stages per warp
+  static constexpr int MINB = (G * HD >= 2048) ? 2 : 3;  // CTAs per SM the register budget aims for
+  static constexpr int RING_B = kNW * NST * 2 * STAGE_B;
   static constexpr int MERGE_B = kNW * G * (HD + 2) * 4;
   static constexpr int AREA_B = RING_B > MERGE_B ? RING_B : MERGE_B;
   // after the area: barriers, per-warp score buffers, cos/sin table, merge weights, flag
   static constexpr int BAR_OFF = AREA_B;
-  static constexpr int SC_OFF = BAR_OFF + kNW * kNST * 8;
-  static constexpr int COS_OFF = SC_OFF + kNW * kNPMax * 4;
+  static constexpr int SC_OFF = BAR_OFF + kNW * NST * 8;
+  static constexpr int SA_OFF = SC_OFF + kNW * kNPMax * 4;
+  static constexpr int COS_OFF = SA_OFF + kNW * 8 * 4;
   static constexpr int W_OFF = COS_OFF + HD * 4;
   static constexpr int FLAG_OFF = W_OFF + G * kMaxSplits * 4;
   static constexpr int SMEM_B = FLAG_OFF + 16;
@@ -189,12 +213,14 @@ __device__ __forceinline__ void norm_rope_row(float* f, const float* w, bool rop
 }
 
 template <typename T, int HD, int G, bool FUSED>
-__global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_constant__ AttnSimtArgs a) {
+__global__ void __launch_bounds__(kNW * 32, (SimtCfg<T, HD, G>::MINB))
+    attn_simt_kernel(const __grid_constant__ AttnSimtArgs a) {
   using C = SimtCfg<T, HD, G>;
   constexpr int EL2 = C::EL / 2;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   float* sc_all = reinterpret_cast<float*>(smem + C::SC_OFF);
+  float* sa_all = reinterpret_cast<float*>(smem + C::SA_OFF);
   float* s_cos = reinterpret_cast<float*>(smem + C::COS_OFF);
   float* s_sin = s_cos + HD / 2;
   float* s_w = reinterpret_cast<float*>(smem + C::W_OFF);
@@ -208,9 +234,9 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
   const int t = bt % a.T;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  uint64_t* wbar = bars + warp * kNST;
+  uint64_t* wbar = bars + warp * C::NST;
   if (lane == 0) {
-    for (int i = 0; i < kNST; ++i) mbar_init(smem_u32(&wbar[i]), 1);
+    for (int i = 0; i < C::NST; ++i) mbar_init(smem_u32(&wbar[i]), 1);
     fence_mbar_init();
   }
   __syncwarp();
@@ -233,9 +259,14 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
   const int nkeys = max(0, k1c - k0);
   const int nstages = (nkeys + C::SK - 1) / C::SK;
 
-  uint8_t* ring = smem + warp * (kNST * 2 * C::STAGE_B);
+  uint8_t* ring = smem + warp * (C::NST * 2 * C::STAGE_B);
   float* sc = sc_all + warp * kNPMax;
+  float* sa = sa_all + warp * 8;
   bool aborted = false;
+  // After a reduce-scatter, lane l holds the score of entry idx = l >> kSh
+  // (key idx / G, head idx % G); it keeps the softmax state (m, l) of head hh.
+  constexpr int kSh = 5 - ilog2(C::NP);
+  const int hh = (lane >> kSh) & (G - 1);
 
   const size_t head_base = (static_cast<size_t>(b) * a.Hkv + kvh) * a.max_len;
   const T* gk = static_cast<const T*>(a.ck) + head_base * HD;
@@ -252,7 +283,7 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
   };
 
   if (lane == 0) {
-    for (int i = 0; i < kNST; ++i) {
+    for (int i = 0; i < C::NST; ++i) {
       const int st = warp + i * kNW;
       if (st < nstages) issue(st, i);
     }
@@ -287,12 +318,10 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
     to_f2<C::EL>(f, q2[h]);
   }
 
-  float m[G], l[G];
+  float m_l = -INFINITY, l_l = 0.0f;  // softmax state of head hh (log2 domain)
   float2 o2[G][EL2];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.0f;
 #pragma unroll
     for (int i = 0; i < EL2; ++i) o2[h][i] = make_float2(0.0f, 0.0f);
   }
@@ -301,8 +330,8 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
   for (int it = 0;; ++it) {
     const int st_idx = warp + it * kNW;
     if (st_idx >= nstages) break;
-    const int buf = it % kNST;
-    if (!warp_wait(smem_u32(&wbar[buf]), (it / kNST) & 1, a.err)) {
+    const int buf = it % C::NST;
+    if (!warp_wait(smem_u32(&wbar[buf]), (it / C::NST) & 1, a.err)) {
       aborted = true;
       break;
     }
@@ -324,40 +353,45 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
         for (int h = 0; h < G; ++h) {
           float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-          for (int i = 0; i < EL2; ++i) acc = __ffma2_rn(q2[h][i], kx[i], acc);
+          for (int i = 0; i < EL2; ++i) acc = fma2(q2[h][i], kx[i], acc);
           part[key * G + h] = acc.x + acc.y;
         }
       }
-      constexpr int kSh = 5 - ilog2(C::NP);  // lanes sharing one reduced score: 1 << kSh
+      // Softmax of this batch: each lane exponentiates its own entry; batch
+      // max and sum per head run over the lanes of the same head (key bits).
       const float s = reduce_scatter<C::NP>(part, lane);
-      if ((lane & ((1 << kSh) - 1)) == 0) sc[lane >> kSh] = s;
-      __syncwarp();
-      float sv_all[C::NP];
+      const int key_l = (lane >> kSh) / G;
+      const float s_me = (kb0 + key_l < n) ? s : -INFINITY;
+      float mb = s_me;
 #pragma unroll
-      for (int i = 0; i < C::NP; ++i) sv_all[i] = sc[i];
+      for (int o = 1 << (kSh + ilog2(G)); o < 32; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+      const float m_new = fmaxf(m_l, mb);
+      const float alpha = (m_l == -INFINITY) ? 0.0f : ex2(m_l - m_new);
+      const float p_l = ex2(s_me - m_new);
+      float ps = p_l;
+#pragma unroll
+      for (int o = 1 << (kSh + ilog2(G)); o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+      l_l = l_l * alpha + ps;
+      m_l = m_new;
+      if ((lane & ((1 << kSh) - 1)) == 0) {
+        sc[lane >> kSh] = p_l;
+        if (key_l == 0) sa[hh] = alpha;
+      }
       __syncwarp();
       float p[C::KB][G];
 #pragma unroll
+      for (int i = 0; i < C::NP; ++i) p[i / G][i % G] = sc[i];
+      float al[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) al[h] = sa[h];
+      __syncwarp();
+#pragma unroll
       for (int h = 0; h < G; ++h) {
-        float mb = -INFINITY;
-#pragma unroll
-        for (int key = 0; key < C::KB; ++key)
-          if (kb0 + key < n) mb = fmaxf(mb, sv_all[key * G + h]);
-        const float m_new = fmaxf(m[h], mb);
-        const float alpha = (m[h] == -INFINITY) ? 0.0f : exp2f(m[h] - m_new);
-        float ps = 0.0f;
-#pragma unroll
-        for (int key = 0; key < C::KB; ++key) {
-          p[key][h] = (kb0 + key < n) ? exp2f(sv_all[key * G + h] - m_new) : 0.0f;
-          ps += p[key][h];
-        }
-        l[h] = l[h] * alpha + ps;
-        m[h] = m_new;
-        if (alpha != 1.0f) {
+        if (al[h] != 1.0f) {
 #pragma unroll
           for (int i = 0; i < EL2; ++i) {
-            o2[h][i].x *= alpha;
-            o2[h][i].y *= alpha;
+            o2[h][i].x *= al[h];
+            o2[h][i].y *= al[h];
           }
         }
       }
@@ -371,14 +405,14 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
           for (int h = 0; h < G; ++h) {
             const float2 pp = make_float2(p[key][h], p[key][h]);
 #pragma unroll
-            for (int i = 0; i < EL2; ++i) o2[h][i] = __ffma2_rn(pp, vx[i], o2[h][i]);
+            for (int i = 0; i < EL2; ++i) o2[h][i] = fma2(pp, vx[i], o2[h][i]);
           }
         }
       }
     }
     __syncwarp();
     consumed = it + 1;
-    const int next = st_idx + kNST * kNW;
+    const int next = st_idx + C::NST * kNW;
     if (lane == 0 && next < nstages) issue(next, buf);
   }
 
@@ -386,8 +420,8 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
   if (aborted) {
     for (int it = consumed;; ++it) {
       const int st_idx = warp + it * kNW;
-      if (st_idx >= nstages || it >= consumed + kNST) break;
-      warp_wait(smem_u32(&wbar[it % kNST]), (it / kNST) & 1, nullptr);
+      if (st_idx >= nstages || it >= consumed + C::NST) break;
+      warp_wait(smem_u32(&wbar[it % C::NST]), (it / C::NST) & 1, nullptr);
     }
   }
 
@@ -410,19 +444,22 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
       for (int h = 0; h < G; ++h) {
         float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-        for (int i = 0; i < EL2; ++i) acc = __ffma2_rn(q2[h][i], kx[i], acc);
+        for (int i = 0; i < EL2; ++i) acc = fma2(q2[h][i], kx[i], acc);
         const float s = warp_sum(acc.x + acc.y);
-        const float m_new = fmaxf(m[h], s);
-        const float alpha = (m[h] == -INFINITY) ? 0.0f : exp2f(m[h] - m_new);
-        const float pn = exp2f(s - m_new);
-        l[h] = l[h] * alpha + pn;
-        m[h] = m_new;
+        const float m_h = __shfl_sync(0xffffffffu, m_l, h << kSh);
+        const float m_new = fmaxf(m_h, s);
+        const float alpha = (m_h == -INFINITY) ? 0.0f : ex2(m_h - m_new);
+        const float pn = ex2(s - m_new);
+        if (hh == h) {
+          l_l = l_l * alpha + pn;
+          m_l = m_new;
+        }
         const float2 pp = make_float2(pn, pn);
 #pragma unroll
         for (int i = 0; i < EL2; ++i) {
           o2[h][i].x *= alpha;
           o2[h][i].y *= alpha;
-          o2[h][i] = __ffma2_rn(pp, vx[i], o2[h][i]);
+          o2[h][i] = fma2(pp, vx[i], o2[h][i]);
         }
       }
     }
@@ -433,12 +470,9 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
   float* ms = reinterpret_cast<float*>(smem);          // [NW][G]
   float* ls = ms + kNW * G;                            // [NW][G]
   float* os = ls + kNW * G;                            // [NW][G][HD]
-  if (lane == 0) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      ms[warp * G + h] = m[h];
-      ls[warp * G + h] = l[h];
-    }
+  if ((lane & ((1 << kSh) - 1)) == 0 && (lane >> kSh) < G) {
+    ms[warp * G + hh] = m_l;
+    ls[warp * G + hh] = l_l;
   }
 #pragma unroll
   for (int h = 0; h < G; ++h) {
@@ -468,7 +502,7 @@ __global__ void __launch_bounds__(kNW * 32) attn_simt_kernel(const __grid_consta
       for (int w = 0; w < kNW; ++w) {
         const float mw = ms[w * G + h];
         if (mw != -INFINITY) {
-          const float f = exp2f(mw - M);
+          const float f = ex2(mw - M);
           O += f * os[(w * G + h) * HD + d];
           Ls += f * ls[w * G + h];
         }
@@ -636,22 +670,49 @@ cudaError_t launch_attn_simt(const AttnSimtArgs& a, int dtype, cudaStream_t s) {
   return dtype == 1 ? launch_simt_t<__nv_bfloat16>(a, s) : launch_simt_t<float>(a, s);
 }
 
+int sm_count() {
+  static int cached[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) {
+    cudaGetLastError();
+    return 152;  // GB300
+  }
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = 152;
+    }
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 DecodePlan decode_plan(int sliding, int window, int hd, int H, int Hkv, int B, int max_seq_len) {
   DecodePlan p;
   const int span = sliding ? (max_seq_len < window ? max_seq_len : window) : max_seq_len;
   const int units = B * Hkv;
-  // Enough CTAs to keep every SM streaming (eight per SM of a 152-SM GPU),
-  // at least 64 keys per split, and at most sqrt(span / 8) splits so that the
-  // final merge (nsplit partials of G*hd floats) stays small next to the
-  // keys each split streams.
-  const int target_ctas = 1216;
-  int nsplit = (target_ctas + units - 1) / units;
+  const int G = H / Hkv;
+  // CTA slots of one wave: SMs x CTAs per SM (two for G*hd >= 2048, else three).
+  const int slots = sm_count() * ((G * hd >= 2048) ? 2 : 3);
+  // Splits: at least 64 keys each, and at most sqrt(span / 8) so that the
+  // final merge (nsplit partials of G*hd floats) stays small next to the keys
+  // each split streams; within that, a whole number of waves (4 down to 1).
   const int by_len = (span + 63) / 64;
   int by_merge = static_cast<int>(sqrt(static_cast<double>(span) / 8.0));
   if (by_merge < 4) by_merge = 4;
-  if (nsplit > by_len) nsplit = by_len;
-  if (nsplit > by_merge) nsplit = by_merge;
-  if (nsplit > kMaxSplits) nsplit = kMaxSplits;
+  int cap = by_len < by_merge ? by_len : by_merge;
+  if (cap > kMaxSplits) cap = kMaxSplits;
+  if (cap < 1) cap = 1;
+  int nsplit = 0;
+  for (int m = 4; m >= 1 && nsplit == 0; --m) {
+    const int ns = static_cast<int>((static_cast<long long>(m) * slots) / units);
+    if (ns >= 1 && ns <= cap) nsplit = ns;
+  }
+  if (nsplit == 0) {
+    const int want = (slots + units - 1) / units;
+    nsplit = want < cap ? want : cap;
+  }
   if (nsplit < 1) nsplit = 1;
   int chunk = (span + nsplit - 1) / nsplit;
   chunk = (chunk + 15) / 16 * 16;

@@ -158,7 +158,7 @@ def g4_decode_step(params, caches, layer, q_in, k_in, v_in, q_norm_w, k_norm_w, 
                                 _ptr(workspace), int(workspace_bytes), _stream(stream, q_in)))
 
 
-G4_NOALLOC_SCRATCH_BYTES = 16 << 20
+G4_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 def g4_attn_decode_noalloc(params, caches, layer, q, seq_lens, B, max_seq_len, out, stream=None):

@@ -216,10 +216,10 @@ g4_status g4_decode_step(const g4_layer_params* params, const g4_kv_cache* cache
 
 /*
  * Bytes of device scratch built into the library for g4_attn_decode_noalloc
- * (16 MiB).  Every GPU that loads the library holds this array until the
+ * (8 MiB).  Every GPU that loads the library holds this array until the
  * process exits.
  */
-#define G4_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+#define G4_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 
 /*
  * g4_attn_decode without a workspace argument, for callers that cannot

@@ -4,7 +4,7 @@ Some callers of this library are handed only their input and output buffers
 -- a plugin inside a host framework that owns every device allocation, or a
 serving loop that must not call cudaMalloc mid-request because it
 synchronises the device and can fail.  For them the library carries a fixed
-16 MiB scratch array in device memory and g4_attn_decode_noalloc uses it in
+8 MiB scratch array in device memory and g4_attn_decode_noalloc uses it in
 place of the caller's workspace.  These tests call it through the C ABI and
 check it against g4_attn_decode (with a caller-allocated workspace) on two
 calls in a row, the second overwriting what the first left in the shared
@@ -96,16 +96,15 @@ def test_no_alloc_decode_matches_workspace_decode_on_two_calls_in_a_row():
 
 
 def test_no_alloc_decode_refuses_plans_beyond_its_scratch():
-    # 1215 sequences of one kv head (group 8, head_dim 256) split in two:
-    # about 1215 * 8 * 2 * (256 + 2) * 4 bytes of partials, more than 16 MiB
+    # many sequences of one kv head (group 8, head_dim 256): find a batch
+    # whose split plan needs more partials than the built-in array holds
     geo = geometry(W.SLIDING, 256, H=8, Hkv=1, window=1024)
     p = params_of(geo)
-    need = G.g4_attn_decode_workspace_size(p, 1215, 1024)
-    assert need > G.G4_NOALLOC_SCRATCH_BYTES
+    B = next(b for b in range(64, 4096, 8) if G.g4_attn_decode_workspace_size(p, b, 1024) > G.G4_NOALLOC_SCRATCH_BYTES)
     fake = 0x7f0000000000
     table = G.cache_table(1)
-    G.set_cache(table, 0, fake, fake + 4096, W.SLIDING, 256, 1, 1024, 1215, W.BF16)
+    G.set_cache(table, 0, fake, fake + 4096, W.SLIDING, 256, 1, 1024, B, W.BF16)
     with pytest.raises(G.G4Error) as e:
-        G.g4_attn_decode_noalloc(p, table, 0, fake, fake, 1215, 1024, fake, stream=0)
+        G.g4_attn_decode_noalloc(p, table, 0, fake, fake, B, 1024, fake, stream=0)
     assert e.value.status == G.G4_ERR_WORKSPACE
     assert "built into the library" in str(e.value)
