@@ -14,8 +14,10 @@
 //               dims) and V chunks (VK keys x DV dims) through a ring of
 //               16 KB shared-memory slots, 128-byte swizzled.
 //   warp 1      allocates TMEM and issues tcgen05.mma (one elected lane):
-//                 S[j%2] = Q K_j^T      (M=128, N=128, K=head_dim; K-major A/B)
-//                 O     += P_j V_j      (M=128, N=DV,  K=128;      V MN-major)
+//                 S[j%2] = Q K_j^T      (M=128, N=128, K=head_dim; A, B from
+//                                        shared memory, K-major)
+//                 O     += P_j V_j      (M=128, N=DV,  K=128; A = P_j from
+//                                        TMEM, B = V_j MN-major)
 //               in the order QK_0, QK_1, PV_0, QK_2, PV_1, ... so the score
 //               MMA of the next tile overlaps the softmax of this one.
 //   warps 2-5   softmax, one query row per thread (TMEM lane = row): load S
@@ -23,9 +25,16 @@
 //               online softmax in the log2 domain with the running maximum
 //               raised only when it grows by more than 2^8 (the stale maximum
 //               is exact for O / l), rescale the O row in TMEM when it is
-//               raised, write P as bf16 into shared memory in the MMA's
-//               swizzled K-major layout, and finally O / l to global memory.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256, 256 + DV).
+//               raised, and write P as bf16 over the first 64 columns of the
+//               same S buffer; finally O / l to global memory.  The row sum
+//               l adds the bf16-rounded P values, the weights the PV MMA
+//               really applies, so a row dominated by one key returns that
+//               key's value without the rounding error of P.
+// TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O [256, 256 + DV).
+// The MMAs of one thread execute in issue order, so QK_{j+2} (issued after
+// PV_j) overwrites P_j only after PV_j has read it; no barrier is needed
+// between them.  Barriers come in pairs indexed by tile parity (j % 2), which
+// keeps each phase unambiguous for waiters that skip phases.
 // Key tiles wholly outside every row's band are never loaded.
 #include <math.h>
 
@@ -39,6 +48,8 @@ constexpr int kBM = 128;       // query rows per CTA
 constexpr int kBN = 128;       // keys per tile
 constexpr int kSlotB = 16384;  // ring slot bytes
 constexpr int kThreads = 192;
+constexpr int kMaxSlots = 12;
+constexpr int kSmemMax = 232448;  // opt-in shared memory per block
 constexpr float kRescaleLog2 = 8.0f;
 
 template <int HD>
@@ -48,27 +59,29 @@ struct TcCfg {
   static constexpr int QCH = HD / 64;             // 64-dim chunks of Q and of a K tile
   static constexpr int VK = 8192 / DV;            // keys per V chunk (VK * DV * 2 = 16 KB)
   static constexpr int VCH = kBN / VK;            // V chunks per tile
-  static constexpr int NSLOT = HD == 512 ? 4 : 8;
   static constexpr int Q_OFF = 0;
-  static constexpr int P_OFF = Q_OFF + QCH * kSlotB;
-  static constexpr int RING_OFF = P_OFF + 2 * kSlotB;
+  static constexpr int RING_OFF = Q_OFF + QCH * kSlotB;
+  static constexpr int BAR_B = 512;
+  static constexpr int NSLOT_FIT = (kSmemMax - 1024 - BAR_B - RING_OFF) / kSlotB;
+  static constexpr int NSLOT = NSLOT_FIT < kMaxSlots ? NSLOT_FIT : kMaxSlots;
   static constexpr int BAR_OFF = RING_OFF + NSLOT * kSlotB;
-  static constexpr int SMEM_B = 1024 + BAR_OFF + 256;  // + alignment slack
-  static_assert(SMEM_B <= 232448, "shared memory budget");
+  static constexpr int SMEM_B = 1024 + BAR_OFF + BAR_B;  // + alignment slack
+  static_assert(NSLOT >= 4, "ring depth");
+  static_assert(SMEM_B <= kSmemMax, "shared memory budget");
 };
 
 struct TcBars {
   uint64_t q_full;
-  uint64_t s_full[2];
-  uint64_t s_free[2];
-  uint64_t p_full;
-  uint64_t o_done;
+  uint64_t s_full[2];  // QK_j complete (tile parity)
+  uint64_t p_full[2];  // P_j written to TMEM by all 128 softmax threads
+  uint64_t o_done[2];  // PV_j complete
   uint64_t drain;
-  uint64_t full[8];
-  uint64_t empty[8];
+  uint64_t full[kMaxSlots];
+  uint64_t empty[kMaxSlots];
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(TcBars) <= 512, "barrier block");
 
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -79,7 +92,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   TcBars* bars = reinterpret_cast<TcBars*>(smem + C::BAR_OFF);
   const uint32_t sQ = smem_u32(smem + C::Q_OFF);
-  const uint32_t sP = smem_u32(smem + C::P_OFF);
   const uint32_t sRing = smem_u32(smem + C::RING_OFF);
   volatile int* abort = &bars->abort;
 
@@ -114,10 +126,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&bars->q_full), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->s_full[i]), 1);
-      mbar_init(smem_u32(&bars->s_free[i]), 128);
+      mbar_init(smem_u32(&bars->p_full[i]), 128);
+      mbar_init(smem_u32(&bars->o_done[i]), 1);
     }
-    mbar_init(smem_u32(&bars->p_full), 128);
-    mbar_init(smem_u32(&bars->o_done), 1);
     mbar_init(smem_u32(&bars->drain), 1);
     for (int i = 0; i < C::NSLOT; ++i) {
       mbar_init(smem_u32(&bars->full[i]), 1);
@@ -202,8 +213,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       auto mma_qk = [&](int j) {
         const int sb = j & 1;
-        if (!warp_wait(smem_u32(&bars->s_free[sb]), ((j >> 1) & 1) ^ 1, a.err, abort)) { ok = false; return; }
-        tc_fence_after();
         const uint32_t dS = tmem + sb * kBN;
         for (int c = 0; c < C::QCH; ++c) {
           const int slot = seq % C::NSLOT;
@@ -225,9 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       };
       auto mma_pv = [&](int j) {
-        if (!warp_wait(smem_u32(&bars->p_full), j & 1, a.err, abort)) { ok = false; return; }
+        const int sb = j & 1;
+        if (!warp_wait(smem_u32(&bars->p_full[sb]), (j >> 1) & 1, a.err, abort)) { ok = false; return; }
         tc_fence_after();
         const int kt = kt_begin + j;
+        const uint32_t tP = tmem + sb * kBN;  // P_j: 128 keys as 64 packed columns
         for (int c = 0; c < C::VCH; ++c) {
           const int slot = seq % C::NSLOT;
           if (!warp_wait(smem_u32(&bars->full[slot]), (seq / C::NSLOT) & 1, a.err, abort)) { ok = false; return; }
@@ -252,16 +263,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < C::VK / 16; ++kk) {
               const int kp = c * C::VK + kk * 16;  // key offset inside the tile
-              const uint64_t ad = smem_desc_sw128(sP + (kp / 64) * kSlotB + ((kp % 64) / 16) * 32, 16, 1024);
               const uint64_t bd = smem_desc_sw128(sRing + slot * kSlotB + kk * 2048, C::VK * 128, 1024);
-              tc_mma_ss(tmem_O, ad, bd, idesc_pv, (j > 0 || c > 0 || kk > 0) ? 1u : 0u);
+              tc_mma_ts(tmem_O, tP + kp / 2, bd, idesc_pv, (j > 0 || c > 0 || kk > 0) ? 1u : 0u);
             }
             tc_commit(smem_u32(&bars->empty[slot]));
           }
           __syncwarp();
           ++seq;
         }
-        if (lane == 0) tc_commit(smem_u32(&bars->o_done));
+        if (lane == 0) tc_commit(smem_u32(&bars->o_done[sb]));
         __syncwarp();
       };
       if (ok) mma_qk(0);
@@ -281,8 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int qpos = qpos_first + r;
     const bool row_valid = r < valid_rows;
-    const float c2 = a.scale_log2;
-    float m = -INFINITY;  // running maximum (log2 units) used as the exponent base
+    const float c2 = a.scale_log2;  // > 0 (checked on the host)
+    float m = -INFINITY;  // exponent base in log2 units: a stale running maximum
     float l = 0.0f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
@@ -291,17 +301,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float s[kBN];
       {
-        uint32_t rr[32];
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        const uint32_t tS = tmem + lane_off + sb * kBN;
+        tmem_ld32(tS, r0);
+        tmem_ld32(tS + 32, r1);
+        tmem_ld32(tS + 64, r2);
+        tmem_ld32(tS + 96, r3);
+        tc_wait_ld();
 #pragma unroll
-        for (int cc = 0; cc < kBN / 32; ++cc) {
-          tmem_ld32(tmem + lane_off + sb * kBN + cc * 32, rr);
-          tc_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(rr[i]) * c2;
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(r0[i]);
+          s[32 + i] = __uint_as_float(r1[i]);
+          s[64 + i] = __uint_as_float(r2[i]);
+          s[96 + i] = __uint_as_float(r3[i]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars->s_free[sb]));
 
       const int k0 = (kt_begin + j) * kBN;
       const bool all_vis = row_valid && (k0 + kBN - 1 <= qpos) && (k0 + kBN <= Lk) &&
@@ -314,9 +328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!vis) s[n] = -INFINITY;
         }
       }
-      float mt = -INFINITY;
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int n = 0; n < kBN; ++n) mt = fmaxf(mt, s[n]);
+      for (int n = 0; n < kBN; ++n) mx[n & 3] = fmaxf(mx[n & 3], s[n]);
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
       float alpha = 1.0f;
       bool rescale = false;
       float m_use = m;
@@ -324,61 +339,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_use = mt;  // nothing accumulated yet (O row is zero or unwritten)
       } else if (mt - m > kRescaleLog2) {
         m_use = mt;
-        alpha = exp2f(m - mt);
+        alpha = ex2_approx(m - mt);
         rescale = true;
       }
-      const float base = (m_use == -INFINITY) ? 0.0f : m_use;
-      float rowsum = 0.0f;
-#pragma unroll
-      for (int n = 0; n < kBN; ++n) {
-        s[n] = exp2f(s[n] - base);
-        rowsum += s[n];
-      }
-      l = l * alpha + rowsum;
-      m = m_use;
-
-      if (j > 0) {
-        // PV of the previous tile has finished: the P buffer is free and O is stable.
-        if (!warp_wait(smem_u32(&bars->o_done), (j - 1) & 1, a.err, abort)) { ok = false; break; }
+      if (__any_sync(0xffffffffu, rescale)) {
+        // A row of this warp raises its base (only after a tile with a
+        // visible key, so j > 0): PV_{j-1} must be complete before the O
+        // rows are scaled; PV_j is not issued until P_j below is published.
+        if (!warp_wait(smem_u32(&bars->o_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, a.err, abort)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
-          const float f = rescale ? alpha : 1.0f;
+        const float f = rescale ? alpha : 1.0f;
 #pragma unroll 1
-          for (int cc = 0; cc < C::DV / 32; ++cc) {
-            uint32_t rr[32];
-            tmem_ld32(tmem_O + lane_off + cc * 32, rr);
-            tc_wait_ld();
+        for (int cc = 0; cc < C::DV / 32; ++cc) {
+          uint32_t rr[32];
+          tmem_ld32(tmem_O + lane_off + cc * 32, rr);
+          tc_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * f);
-            tmem_st32(tmem_O + lane_off + cc * 32, rr);
-          }
-          tc_wait_st();
+          for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * f);
+          tmem_st32(tmem_O + lane_off + cc * 32, rr);
         }
+        tc_wait_st();
       }
-      // P row r as bf16, K-major with the 128-byte swizzle: 16-byte chunk ch
-      // of the row's 128-byte line lands at chunk ch ^ (r % 8).
+      const float nb = (m_use == -INFINITY) ? 0.0f : -m_use;
+      uint32_t p0[32], p1[32];
+      float sa[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const int n0 = half * 64 + ch * 8;
-          uint4 v;
-          v.x = pack_bf16x2(s[n0 + 0], s[n0 + 1]);
-          v.y = pack_bf16x2(s[n0 + 2], s[n0 + 3]);
-          v.z = pack_bf16x2(s[n0 + 4], s[n0 + 5]);
-          v.w = pack_bf16x2(s[n0 + 6], s[n0 + 7]);
-          const uint32_t addr = sP + half * kSlotB + r * 128 + ((ch ^ (r & 7)) * 16);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-                       "r"(v.w)
-                       : "memory");
-        }
+      for (int i = 0; i < 32; ++i) {
+        const uint32_t w0 = pack_bf16x2(ex2_approx(fmaf(s[2 * i], c2, nb)), ex2_approx(fmaf(s[2 * i + 1], c2, nb)));
+        const uint32_t w1 =
+            pack_bf16x2(ex2_approx(fmaf(s[64 + 2 * i], c2, nb)), ex2_approx(fmaf(s[64 + 2 * i + 1], c2, nb)));
+        p0[i] = w0;
+        p1[i] = w1;
+        sa[0] += bf16_lo(w0);
+        sa[1] += bf16_hi(w0);
+        sa[2] += bf16_lo(w1);
+        sa[3] += bf16_hi(w1);
       }
-      fence_proxy_async_smem();
+      tmem_st32(tmem + lane_off + sb * kBN, p0);
+      tmem_st32(tmem + lane_off + sb * kBN + 32, p1);
+      l = l * alpha + ((sa[0] + sa[1]) + (sa[2] + sa[3]));
+      m = m_use;
+      tc_wait_st();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bars->p_full));
+      mbar_arrive(smem_u32(&bars->p_full[sb]));
     }
     if (ntiles > 0 && ok) {
-      if (warp_wait(smem_u32(&bars->o_done), (ntiles - 1) & 1, a.err, abort)) {
+      const int jl = ntiles - 1;
+      if (warp_wait(smem_u32(&bars->o_done[jl & 1]), (jl >> 1) & 1, a.err, abort)) {
         tc_fence_after();
         const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
