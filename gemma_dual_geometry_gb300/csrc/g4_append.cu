@@ -11,29 +11,28 @@
 //
 // One CTA (4 warps) per token handles rows_per_cta of its H + 2*Hkv head
 // rows; one warp per head row.  The token's cos/sin table (head_dim / 2
-// pairs) is built once per CTA: angle = pos * inv_freq[j] with inv_freq a
-// float32 table, reduced modulo 2*pi in float64 (exact product, one fma), then
-// sincosf of the reduced float angle.  Pairs j >= n_rot (zero inv_freq) are
-// left untouched, so those dims are the normed input bit for bit.
+// pairs, double-float) is built once per CTA from angle = pos * inv_freq[j]
+// with inv_freq a float32 table.  Pairs j >= n_rot (zero inv_freq) are left
+// unrotated, so those dims are the normed input.  bf16 stores are the
+// correctly rounded real results (g4_normrope.cuh).
 //
 // Lane l of a warp owns elements [l*E, l*E + E) of the lower half and the
 // same offsets of the upper half (E = head_dim / 64), so each rotate_half
 // pair (j, j + head_dim/2) sits in one lane.
 #include "g4_device.cuh"
 #include "g4_internal.h"
+#include "g4_normrope.cuh"
 
 namespace g4 {
 namespace {
-
-constexpr double kInv2Pi = 0.15915494309189533576888376337251;  // 1 / (2 pi)
-constexpr double k2Pi = 6.2831853071795864769252867665590;      // 2 pi
 
 template <typename T, int HD>
 __global__ void __launch_bounds__(128) append_normrope_kernel(const __grid_constant__ AppendArgs a) {
   constexpr int HALF = HD / 2;
   constexpr int E = HD / 64;
-  __shared__ float s_cos[HALF];
-  __shared__ float s_sin[HALF];
+  constexpr bool kBF16 = sizeof(T) == 2;
+  __shared__ DF s_cos[HALF];
+  __shared__ DF s_sin[HALF];
 
   pdl_wait();
   pdl_trigger();
@@ -42,13 +41,8 @@ __global__ void __launch_bounds__(128) append_normrope_kernel(const __grid_const
   const int pos = a.positions[tok];
 
   for (int j = threadIdx.x; j < HALF; j += blockDim.x) {
-    float c = 1.0f, s = 0.0f;
-    if (j < a.n_rot) {
-      const double ang = static_cast<double>(pos) * static_cast<double>(a.inv_freq[j]);
-      const double k = rint(ang * kInv2Pi);
-      const double r = fma(-k, k2Pi, ang);
-      sincosf(static_cast<float>(r), &s, &c);
-    }
+    DF c = {1.0f, 0.0f}, s = {0.0f, 0.0f};
+    if (j < a.n_rot) sincos_df(pos, a.inv_freq[j], c, s);
     s_cos[j] = c;
     s_sin[j] = s;
   }
@@ -83,38 +77,22 @@ __global__ void __launch_bounds__(128) append_normrope_kernel(const __grid_const
       w = is_k ? a.k_w : nullptr;
       rope = is_k;
     }
-    float x[2 * E];
+    float x[2 * E], wl[E], wh[E];
     load_elems<E>(src + lane * E, x);
     load_elems<E>(src + HALF + lane * E, x + E);
-    float ss = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 2 * E; ++i) ss = fmaf(x[i], x[i], ss);
-    ss = warp_sum(ss);
-    const float inv = 1.0f / sqrtf(ss / static_cast<float>(HD) + a.eps);
     if (w != nullptr) {
-      float wl[E], wh[E];
       load_elems<E>(w + lane * E, wl);
       load_elems<E>(w + HALF + lane * E, wh);
-#pragma unroll
-      for (int i = 0; i < E; ++i) {
-        x[i] = x[i] * inv * wl[i];
-        x[E + i] = x[E + i] * inv * wh[i];
-      }
     } else {
 #pragma unroll
-      for (int i = 0; i < 2 * E; ++i) x[i] *= inv;
+      for (int i = 0; i < E; ++i) wl[i] = wh[i] = 1.0f;
     }
-    if (rope) {
+    const DF r = inv_rms_df(row_sumsq_df<2 * E>(x), HD, a.eps);
 #pragma unroll
-      for (int i = 0; i < E; ++i) {
-        const int j = lane * E + i;
-        if (j < a.n_rot) {
-          const float c = s_cos[j], s = s_sin[j];
-          const float lo = x[i], hi = x[E + i];
-          x[i] = lo * c - hi * s;
-          x[E + i] = hi * c + lo * s;
-        }
-      }
+    for (int i = 0; i < E; ++i) {
+      const int j = lane * E + i;
+      const bool rot = rope && j < a.n_rot;
+      normrope_pair<kBF16>(x[i], wl[i], x[E + i], wh[i], r, rot, s_cos[j], s_sin[j], x[i], x[E + i]);
     }
     store_elems<E>(dst + lane * E, x);
     store_elems<E>(dst + HALF + lane * E, x + E);

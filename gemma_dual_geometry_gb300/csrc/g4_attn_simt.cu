@@ -40,6 +40,7 @@
 
 #include "g4_device.cuh"
 #include "g4_internal.h"
+#include "g4_normrope.cuh"
 
 namespace g4 {
 namespace {
@@ -47,8 +48,8 @@ namespace {
 constexpr int kNW = 4;            // warps per CTA
 constexpr int kNPMax = 16;        // partial scores per reduce-scatter batch, at most
 constexpr int kStageMaxB = 4096;  // bytes of K (and of V) a reduce batch may span
-constexpr double kInv2Pi = 0.15915494309189533576888376337251;  // 1 / (2 pi)
-constexpr double k2Pi = 6.2831853071795864769252867665590;      // 2 pi
+
+
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
 
@@ -118,7 +119,7 @@ struct SimtCfg {
   static constexpr int SC_OFF = BAR_OFF + kNW * NST * 8;
   static constexpr int SA_OFF = SC_OFF + kNW * kNPMax * 4;
   static constexpr int COS_OFF = SA_OFF + kNW * 8 * 4;
-  static constexpr int W_OFF = COS_OFF + HD * 4;
+  static constexpr int W_OFF = COS_OFF + HD * 8;  // cos and sin, double-float, HD/2 pairs
   static constexpr int FLAG_OFF = W_OFF + G * kMaxSplits * 4;
   static constexpr int SMEM_B = FLAG_OFF + 16;
   static_assert(NP >= 2 && NP <= 16 && (NP & (NP - 1)) == 0, "reduce batch");
@@ -163,53 +164,57 @@ __device__ __forceinline__ float through(float x) {
 
 // RMSNorm (optional weight) then rotate_half RoPE of one row held in the lane
 // layout above; the partner of element d is d +- HD/2, which is the same lane
-// (NPC >= 2) or lane ^ 16 (NPC == 1).  Result rounded through T.
+// (NPC >= 2) or lane ^ 16 (NPC == 1).  bf16 results are the correctly rounded
+// real values (g4_normrope.cuh), the same the append kernel stores.
 template <typename T, int HD, int NPC, int PE>
-__device__ __forceinline__ void norm_rope_row(float* f, const float* w, bool rope, const float* s_cos,
-                                              const float* s_sin, int n_rot, float eps, int lane) {
+__device__ __forceinline__ void norm_rope_row(float* f, const float* w, bool rope, const DF* s_cos, const DF* s_sin,
+                                              int n_rot, float eps, int lane) {
   constexpr int EL = NPC * PE;
-  float ss = 0.0f;
-#pragma unroll
-  for (int i = 0; i < EL; ++i) ss = fmaf(f[i], f[i], ss);
-  ss = warp_sum(ss);
-  const float inv = 1.0f / sqrtf(ss / static_cast<float>(HD) + eps);
+  constexpr bool kBF16 = sizeof(T) == 2;
+  const DF r = inv_rms_df(row_sumsq_df<EL>(f), HD, eps);
+  float wf[EL];
   if (w != nullptr) {
-    float wf[EL];
     load_row<float, NPC, PE>(w, lane, wf);
-#pragma unroll
-    for (int i = 0; i < EL; ++i) f[i] = f[i] * inv * wf[i];
   } else {
 #pragma unroll
-    for (int i = 0; i < EL; ++i) f[i] *= inv;
+    for (int i = 0; i < EL; ++i) wf[i] = 1.0f;
   }
-  if (rope) {
-    float fp[EL];
-    if constexpr (NPC >= 2) {
+  // raw partner values and weights
+  float fp[EL], wp[EL];
+  if constexpr (NPC >= 2) {
 #pragma unroll
-      for (int c = 0; c < NPC; ++c)
-#pragma unroll
-        for (int e = 0; e < PE; ++e) fp[c * PE + e] = f[((c + NPC / 2) % NPC) * PE + e];
-    } else {
-#pragma unroll
-      for (int e = 0; e < PE; ++e) fp[e] = __shfl_xor_sync(0xffffffffu, f[e], 16);
-    }
-#pragma unroll
-    for (int c = 0; c < NPC; ++c) {
+    for (int c = 0; c < NPC; ++c)
 #pragma unroll
       for (int e = 0; e < PE; ++e) {
-        const int d = (lane + 32 * c) * PE + e;
-        const bool lower = d < HD / 2;
-        const int j = lower ? d : d - HD / 2;
-        if (j < n_rot) {
-          const float cs = s_cos[j], sn = s_sin[j];
-          const float x = f[c * PE + e], y = fp[c * PE + e];
-          f[c * PE + e] = lower ? (x * cs - y * sn) : (x * cs + y * sn);
-        }
+        fp[c * PE + e] = f[((c + NPC / 2) % NPC) * PE + e];
+        wp[c * PE + e] = wf[((c + NPC / 2) % NPC) * PE + e];
+      }
+  } else {
+#pragma unroll
+    for (int e = 0; e < PE; ++e) {
+      fp[e] = __shfl_xor_sync(0xffffffffu, f[e], 16);
+      wp[e] = __shfl_xor_sync(0xffffffffu, wf[e], 16);
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < NPC; ++c) {
+#pragma unroll
+    for (int e = 0; e < PE; ++e) {
+      const int i = c * PE + e;
+      const int d = (lane + 32 * c) * PE + e;
+      const bool lower = d < HD / 2;
+      const int j = lower ? d : d - HD / 2;
+      const bool rot = rope && j < n_rot;
+      float oa, ob;
+      if (lower) {
+        normrope_pair<kBF16>(f[i], wf[i], fp[i], wp[i], r, rot, s_cos[j], s_sin[j], oa, ob);
+        f[i] = oa;
+      } else {
+        normrope_pair<kBF16>(fp[i], wp[i], f[i], wf[i], r, rot, s_cos[j], s_sin[j], oa, ob);
+        f[i] = ob;
       }
     }
   }
-#pragma unroll
-  for (int i = 0; i < EL; ++i) f[i] = through<T>(f[i]);
 }
 
 template <typename T, int HD, int G, bool FUSED>
@@ -221,8 +226,8 @@ __global__ void __launch_bounds__(kNW * 32, (SimtCfg<T, HD, G>::MINB))
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   float* sc_all = reinterpret_cast<float*>(smem + C::SC_OFF);
   float* sa_all = reinterpret_cast<float*>(smem + C::SA_OFF);
-  float* s_cos = reinterpret_cast<float*>(smem + C::COS_OFF);
-  float* s_sin = s_cos + HD / 2;
+  DF* s_cos = reinterpret_cast<DF*>(smem + C::COS_OFF);
+  DF* s_sin = s_cos + HD / 2;
   float* s_w = reinterpret_cast<float*>(smem + C::W_OFF);
   int* s_flag = reinterpret_cast<int*>(smem + C::FLAG_OFF);
 
@@ -290,15 +295,11 @@ __global__ void __launch_bounds__(kNW * 32, (SimtCfg<T, HD, G>::MINB))
   }
 
   if constexpr (FUSED) {
-    // cos/sin of the new token's position, angle reduced in float64
+    // cos/sin of the new token's position (double-float)
     const int pos = L - 1;
     for (int j = threadIdx.x; j < HD / 2; j += blockDim.x) {
-      float c = 1.0f, s = 0.0f;
-      if (j < a.n_rot) {
-        const double ang = static_cast<double>(pos) * static_cast<double>(a.inv_freq[j]);
-        const double k = rint(ang * kInv2Pi);
-        sincosf(static_cast<float>(fma(-k, k2Pi, ang)), &s, &c);
-      }
+      DF c = {1.0f, 0.0f}, s = {0.0f, 0.0f};
+      if (j < a.n_rot) sincos_df(pos, a.inv_freq[j], c, s);
       s_cos[j] = c;
       s_sin[j] = s;
     }

@@ -1,0 +1,222 @@
+// Per-head RMSNorm + rotate_half RoPE of one element pair, with the bf16
+// stored value rounded correctly from the real-number result.
+//
+// What is computed (cortiq-engine g4e.rs `rms` / `rms_plain`, taconite
+// model.rs `rope_half`): for a head row x of width hd with weight w,
+//   y_d  = x_d * (mean(x^2) + eps)^(-1/2) * w_d          (w = 1 for V)
+//   y'_j = y_j cos(p f_j) - y_{j+hd/2} sin(p f_j)
+//   y'_{j+hd/2} = y_{j+hd/2} cos(p f_j) + y_j sin(p f_j)  for j < n_rot
+// with f_j the float32 inverse frequency and p the token position.
+//
+// Storing y' as bf16 is a rounding decision, and a one-ulp difference in a
+// stored q or k moves a score of a scale-1.0 softmax enough to change an
+// attention output by more than its own rounding.  So the stored bf16 value
+// is the round-to-nearest-even of the exact result:
+//   * a float32 evaluation runs first, with a bound on its error; when no
+//     bf16 rounding boundary lies within that bound of the float32 value, its
+//     rounding is the correct one (Ziv's rounding test);
+//   * otherwise a double-float evaluation decides: values carried as an
+//     unevaluated sum of two floats, built from Dekker's exact product (one
+//     fma) and Knuth's two-sum, accurate to about 2^-44 relative.
+// The row's sum of squares and inverse root, and cos / sin of every rotated
+// pair, are always kept in double-float; cos / sin come from Cody-Waite
+// reduction by a three-float pi/2 and Taylor polynomials on [-pi/4, pi/4].
+#pragma once
+
+#include "g4_device.cuh"
+
+namespace g4 {
+
+// h + l with |l| <= ulp(h) / 2.
+struct DF {
+  float h, l;
+};
+
+// a + b = s + e exactly (Knuth).
+__device__ __forceinline__ DF two_sum(float a, float b) {
+  const float s = a + b;
+  const float bb = s - a;
+  return {s, (a - (s - bb)) + (b - bb)};
+}
+
+// a + b = s + e exactly when |a| >= |b| or a == 0 (Dekker).
+__device__ __forceinline__ DF fast_two_sum(float a, float b) {
+  const float s = a + b;
+  return {s, b - (s - a)};
+}
+
+// a * b = p + e exactly (the fma returns the product's rounding error).
+__device__ __forceinline__ DF two_prod(float a, float b) {
+  const float p = a * b;
+  return {p, fmaf(a, b, -p)};
+}
+
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const DF s = two_sum(a.h, b.h);
+  return fast_two_sum(s.h, s.l + (a.l + b.l));
+}
+
+__device__ __forceinline__ DF df_add_f(DF a, float b) {
+  const DF s = two_sum(a.h, b);
+  return fast_two_sum(s.h, s.l + a.l);
+}
+
+__device__ __forceinline__ DF df_mul(DF a, DF b) {
+  const DF p = two_prod(a.h, b.h);
+  return fast_two_sum(p.h, fmaf(a.h, b.l, fmaf(a.l, b.h, p.l)));
+}
+
+__device__ __forceinline__ DF df_mul_f(DF a, float b) {
+  const DF p = two_prod(a.h, b);
+  return fast_two_sum(p.h, fmaf(a.l, b, p.l));
+}
+
+__device__ __forceinline__ DF df_neg(DF a) { return {-a.h, -a.l}; }
+
+// The exact bf16 round-to-nearest-even of h + l, returned as a float.
+__device__ __forceinline__ float df_round_bf16(DF v) {
+  const uint32_t b = __float_as_uint(v.h);
+  if ((b & 0xFFFFu) == 0x8000u && v.l != 0.0f) {
+    // h sits exactly on a bf16 midpoint: the sign of l decides.
+    const bool away = (v.l > 0.0f) == (v.h > 0.0f);
+    return __uint_as_float((b & 0xFFFF0000u) + (away ? 0x10000u : 0u));
+  }
+  return __bfloat162float(__float2bfloat16_rn(v.h));
+}
+
+// The bf16 rounding boundary of v's bf16 interval (same sign and binade as v,
+// so v - mid is exact).
+__device__ __forceinline__ float bf16_midpoint(float v) {
+  return __uint_as_float((__float_as_uint(v) & 0xFFFF0000u) | 0x8000u);
+}
+
+// Row sum of squares in double-float over the lane's n elements, then over
+// the 32 lanes of the warp (every lane ends with the same value).
+template <int N>
+__device__ __forceinline__ DF row_sumsq_df(const float* x) {
+  float hi = 0.0f, lo = 0.0f;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const DF p = two_prod(x[i], x[i]);
+    const DF t = two_sum(hi, p.h);
+    hi = t.h;
+    lo += t.l + p.l;
+  }
+  DF s = fast_two_sum(hi, lo);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const DF t = {__shfl_xor_sync(0xffffffffu, s.h, o), __shfl_xor_sync(0xffffffffu, s.l, o)};
+    s = df_add(s, t);  // symmetric in its arguments, so all lanes agree
+  }
+  return s;
+}
+
+// (sumsq / hd + eps)^(-1/2) in double-float: one Newton step on rsqrtf.
+__device__ __forceinline__ DF inv_rms_df(DF sumsq, int hd, float eps) {
+  const float inv_hd = 1.0f / static_cast<float>(hd);  // hd is a power of two: exact
+  const DF ms = df_add_f(DF{sumsq.h * inv_hd, sumsq.l * inv_hd}, eps);
+  const float r0 = rsqrtf(ms.h);
+  const DF t = df_mul(ms, two_prod(r0, r0));  // ms * r0^2, close to 1
+  const float d = (1.0f - t.h) - t.l;         // 1 - t.h is exact there
+  return fast_two_sum(r0, r0 * (0.5f * d));
+}
+
+// cos and sin of p * f (p an integer position, f a float32 frequency) in
+// double-float.
+__device__ __forceinline__ void sincos_df(int p, float f, DF& c_out, DF& s_out) {
+  DF r;
+  int quadrant;
+  if (p < (1 << 24)) {
+    // theta = p * f exactly (p is exact in float); k = nearest multiple of pi/2
+    const DF th = two_prod(static_cast<float>(p), f);
+    const float k = rintf(th.h * 0x1.45f306p-1f);  // 2 / pi
+    // pi/2 = P1 + P2 + P3 (+ < 1e-23)
+    constexpr float P1 = 0x1.921fb6p+0f, P2 = -0x1.777a5cp-25f, P3 = -0x1.ee59dap-50f;
+    const DF a = two_prod(k, P1);
+    const float r_hi = th.h - a.h;  // exact: th.h and k * P1 are within a factor of two (or k = 0)
+    DF e = two_sum(th.l, -a.l);
+    e = df_add(e, df_neg(two_prod(k, P2)));
+    e = df_add_f(e, -k * P3);
+    r = df_add_f(e, r_hi);
+    quadrant = static_cast<int>(k) & 3;
+  } else {
+    // positions beyond float's exact integers: reduce in float64
+    const double th = static_cast<double>(p) * static_cast<double>(f);
+    const double k = rint(th * 0.63661977236758134308);
+    const double rd = fma(-k, 1.5707963267948966192e0, th) - k * 6.123233995736766036e-17;
+    r.h = static_cast<float>(rd);
+    r.l = static_cast<float>(rd - static_cast<double>(r.h));
+    quadrant = static_cast<int>(fmod(k, 4.0) + 4.0) & 3;
+  }
+  // Taylor polynomials on |r| <= pi/4 (+ a rounding of k): the leading
+  // coefficients 1/n! in double-float, the tail (< 2^-30 of the result) in float.
+  const DF z = df_mul(r, r);
+  const float zh = z.h;
+  // sin r = r + r z S(z), S(z) = -1/3! + z/5! - z^2/7! + z^3/9! - z^4/11! + z^5/13! - z^6/15!
+  float ts = fmaf(zh, -0x1.ae7f3ep-41f, 0x1.612462p-33f);
+  ts = fmaf(zh, ts, -0x1.ae6456p-26f);
+  DF S = df_add(df_mul_f(z, ts), DF{0x1.71de3ap-19f, 0x1.55b1ccp-45f});
+  S = df_add(df_mul(z, S), DF{-0x1.a01a02p-13f, 0x1.7f97fap-39f});
+  S = df_add(df_mul(z, S), DF{0x1.111112p-7f, -0x1.dddddep-32f});
+  S = df_add(df_mul(z, S), DF{-0x1.555556p-3f, 0x1.555556p-28f});
+  const DF sn = df_add(r, df_mul(df_mul(r, z), S));
+  // cos r = 1 - z/2 + z^2 C(z), C(z) = 1/4! - z/6! + z^2/8! - z^3/10! + z^4/12! - z^5/14! + z^6/16!
+  float tc = fmaf(zh, 0x1.ae7f3ep-45f, -0x1.93974ap-37f);
+  tc = fmaf(zh, tc, 0x1.1eed8ep-29f);
+  DF Cz = df_add(df_mul_f(z, tc), DF{-0x1.27e4fcp-22f, 0x1.10ec14p-47f});
+  Cz = df_add(df_mul(z, Cz), DF{0x1.a01a02p-16f, -0x1.7f97fap-42f});
+  Cz = df_add(df_mul(z, Cz), DF{-0x1.6c16c2p-10f, 0x1.27d27ep-35f});
+  Cz = df_add(df_mul(z, Cz), DF{0x1.555556p-5f, -0x1.555556p-30f});
+  const DF cs = df_add(df_add_f(DF{-0.5f * z.h, -0.5f * z.l}, 1.0f), df_mul(df_mul(z, z), Cz));
+  // theta = k pi/2 + r
+  switch (quadrant) {
+    case 0: c_out = cs; s_out = sn; break;
+    case 1: c_out = df_neg(sn); s_out = cs; break;
+    case 2: c_out = df_neg(cs); s_out = df_neg(sn); break;
+    default: c_out = sn; s_out = df_neg(cs); break;
+  }
+}
+
+// The float32 evaluation of one output is off from the exact value by at
+// most 6u (|y_a| + |y_b|), u = 2^-24 (three roundings in y, one in cos / sin,
+// one in the product, one in the fma); the test uses twice that.
+constexpr float kNormRopeErr = 12.0f * 0x1.0p-24f;
+
+// Exact value of one output of a pair, rounded to bf16: y_self * c +- y_other
+// * s on a rotated pair (sign - for the lower element), else y_self.
+static __device__ __noinline__ float normrope_exact_bf16(float x_self, float w_self, float x_other, float w_other, DF r,
+                                                  bool rot, bool lower, DF c, DF s) {
+  const DF ys = df_mul_f(df_mul_f(r, x_self), w_self);
+  if (!rot) return df_round_bf16(ys);
+  const DF yo = df_mul_f(df_mul_f(r, x_other), w_other);
+  return df_round_bf16(df_add(df_mul(ys, c), df_mul(yo, lower ? df_neg(s) : s)));
+}
+
+// One pair (lower a = element j, upper b = element j + hd/2) of a row whose
+// inverse rms is r.  Returns the two outputs as floats; with BF16 set they
+// are exactly the correctly rounded bf16 values, else float32 results.
+template <bool BF16>
+__device__ __forceinline__ void normrope_pair(float xa, float wa, float xb, float wb, DF r, bool rot, DF c, DF s,
+                                              float& oa, float& ob) {
+  const float ya = (xa * r.h) * wa;
+  const float yb = (xb * r.h) * wb;
+  float ea, eb;
+  if (rot) {
+    oa = fmaf(ya, c.h, -(yb * s.h));
+    ob = fmaf(yb, c.h, ya * s.h);
+    ea = eb = kNormRopeErr * (fabsf(ya) + fabsf(yb));
+  } else {
+    oa = ya;
+    ob = yb;
+    ea = kNormRopeErr * fabsf(ya);
+    eb = kNormRopeErr * fabsf(yb);
+  }
+  if constexpr (BF16) {
+    if (fabsf(oa - bf16_midpoint(oa)) > ea) oa = __bfloat162float(__float2bfloat16_rn(oa));
+    else oa = normrope_exact_bf16(xa, wa, xb, wb, r, rot, true, c, s);
+    if (fabsf(ob - bf16_midpoint(ob)) > eb) ob = __bfloat162float(__float2bfloat16_rn(ob));
+    else ob = normrope_exact_bf16(xb, wb, xa, wa, r, rot, false, c, s);
+  }
+}
+
+}  // namespace g4
