@@ -22,7 +22,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libg4attn.so")
 SOURCES = ["g4_api.cu", "g4_append.cu", "g4_attn_simt.cu", "g4_prefill_tc.cu"]
-HEADERS = ["g4_device.cuh", "g4_internal.h"]
+HEADERS = ["g4_device.cuh", "g4_internal.h", "g4_normrope.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -197,7 +197,11 @@ g4_status g4_kv_append_normrope(const g4_layer_params* params, const g4_kv_cache
   a.hd = params->head_dim;
   a.eps = params->eps;
   const int nrows = a.H + (shared ? 0 : 2 * a.Hkv);
-  a.rows_per_cta = (static_cast<long long>(B) * T >= 1024) ? nrows : 4;
+  // Tokens at the same t of up to 8 sequences share a CTA (and, when their
+  // positions agree, one cos/sin table); small launches split the rows.
+  a.tok_per_cta = T >= 16 ? (B < 8 ? B : 8) : 1;
+  const long long ctas = static_cast<long long>(T) * ((B + a.tok_per_cta - 1) / a.tok_per_cta);
+  a.rows_per_cta = ctas >= 1024 ? nrows : 4;
   // inv_freq[j] = theta^(-2j/hd) in float64, stored as float32; zero past the rotated pairs.
   const int half = a.hd / 2;
   int n_rot = static_cast<int>(floor(static_cast<double>(a.hd) * static_cast<double>(params->rotary_fraction) / 2.0));

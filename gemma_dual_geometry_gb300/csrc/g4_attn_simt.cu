@@ -119,9 +119,10 @@ struct SimtCfg {
   static constexpr int SC_OFF = BAR_OFF + kNW * NST * 8;
   static constexpr int SA_OFF = SC_OFF + kNW * kNPMax * 4;
   static constexpr int COS_OFF = SA_OFF + kNW * 8 * 4;
-  static constexpr int W_OFF = COS_OFF + HD * 8;  // cos and sin, double-float, HD/2 pairs
+  static constexpr int W_OFF = COS_OFF + HD * 8;  // cos and sin of HD/2 pairs, double-float
   static constexpr int FLAG_OFF = W_OFF + G * kMaxSplits * 4;
-  static constexpr int SMEM_B = FLAG_OFF + 16;
+  static constexpr int QN_OFF = FLAG_OFF + 16;  // normed q of the G heads (fused step)
+  static constexpr int SMEM_B = QN_OFF + G * HD * ES;
   static_assert(NP >= 2 && NP <= 16 && (NP & (NP - 1)) == 0, "reduce batch");
   static_assert(SMEM_B <= 232448, "shared memory budget");
 };
@@ -163,15 +164,18 @@ __device__ __forceinline__ float through(float x) {
 }
 
 // RMSNorm (optional weight) then rotate_half RoPE of one row held in the lane
-// layout above; the partner of element d is d +- HD/2, which is the same lane
-// (NPC >= 2) or lane ^ 16 (NPC == 1).  bf16 results are the correctly rounded
-// real values (g4_normrope.cuh), the same the append kernel stores.
+// layout above, at position pos; the partner of element d is d +- HD/2, which
+// is the same lane (NPC >= 2) or lane ^ 16 (NPC == 1).  bf16 results are the
+// correctly rounded real values (g4_normrope.cuh), the ones the append
+// kernel stores.  s_cos / s_sin hold cos and sin of the HD/2 pairs.
 template <typename T, int HD, int NPC, int PE>
 __device__ __forceinline__ void norm_rope_row(float* f, const float* w, bool rope, const DF* s_cos, const DF* s_sin,
                                               int n_rot, float eps, int lane) {
   constexpr int EL = NPC * PE;
   constexpr bool kBF16 = sizeof(T) == 2;
-  const DF r = inv_rms_df(row_sumsq_df<EL>(f), HD, eps);
+  constexpr float kErrY = normrope_err_y<EL>();
+  constexpr float kErrRot = normrope_err_rot<EL>(kDFTrigErrUnits);
+  const float r = inv_rms_f32(row_sumsq_f32<EL>(f), HD, eps);
   float wf[EL];
   if (w != nullptr) {
     load_row<float, NPC, PE>(w, lane, wf);
@@ -196,6 +200,8 @@ __device__ __forceinline__ void norm_rope_row(float* f, const float* w, bool rop
       wp[e] = __shfl_xor_sync(0xffffffffu, wf[e], 16);
     }
   }
+  float o[EL];
+  uint32_t need = 0;
 #pragma unroll
   for (int c = 0; c < NPC; ++c) {
 #pragma unroll
@@ -205,16 +211,41 @@ __device__ __forceinline__ void norm_rope_row(float* f, const float* w, bool rop
       const bool lower = d < HD / 2;
       const int j = lower ? d : d - HD / 2;
       const bool rot = rope && j < n_rot;
+      const float2 t = rot ? make_float2(s_cos[j].h, s_sin[j].h) : make_float2(1.0f, 0.0f);
       float oa, ob;
+      bool na, nb;
       if (lower) {
-        normrope_pair<kBF16>(f[i], wf[i], fp[i], wp[i], r, rot, s_cos[j], s_sin[j], oa, ob);
-        f[i] = oa;
+        normrope_pair_fast(f[i], wf[i], fp[i], wp[i], r, rot, t.x, t.y, kErrY, kErrRot, oa, ob, na, nb);
+        o[i] = oa;
+        need |= (na ? 1u : 0u) << i;
       } else {
-        normrope_pair<kBF16>(fp[i], wp[i], f[i], wf[i], r, rot, s_cos[j], s_sin[j], oa, ob);
-        f[i] = ob;
+        normrope_pair_fast(fp[i], wp[i], f[i], wf[i], r, rot, t.x, t.y, kErrY, kErrRot, oa, ob, na, nb);
+        o[i] = ob;
+        need |= (nb ? 1u : 0u) << i;
       }
     }
   }
+  if constexpr (kBF16) {
+    if (__any_sync(0xffffffffu, need != 0)) {
+      const DF rd = inv_rms_df(row_sumsq_df<EL>(f), HD, eps);
+#pragma unroll
+      for (int c = 0; c < NPC; ++c) {
+#pragma unroll
+        for (int e = 0; e < PE; ++e) {
+          const int i = c * PE + e;
+          if (need & (1u << i)) {
+            const int d = (lane + 32 * c) * PE + e;
+            const bool lower = d < HD / 2;
+            const int j = lower ? d : d - HD / 2;
+            o[i] = normrope_exact_bf16(f[i], wf[i], fp[i], wp[i], rd, rope && j < n_rot, lower, s_cos[j], s_sin[j]);
+          }
+        }
+      }
+    }
+  }
+  // the stored value (certified float32 values still need their rounding)
+#pragma unroll
+  for (int i = 0; i < EL; ++i) f[i] = through<T>(o[i]);
 }
 
 template <typename T, int HD, int G, bool FUSED>
@@ -295,7 +326,8 @@ __global__ void __launch_bounds__(kNW * 32, (SimtCfg<T, HD, G>::MINB))
   }
 
   if constexpr (FUSED) {
-    // cos/sin of the new token's position (double-float)
+    // cos/sin of the new token's position, then its q heads normed and
+    // roped once per CTA (warp w takes heads w, w + 4, ...) into shared memory
     const int pos = L - 1;
     for (int j = threadIdx.x; j < HD / 2; j += blockDim.x) {
       DF c = {1.0f, 0.0f}, s = {0.0f, 0.0f};
@@ -304,16 +336,25 @@ __global__ void __launch_bounds__(kNW * 32, (SimtCfg<T, HD, G>::MINB))
       s_sin[j] = s;
     }
     __syncthreads();
+    T* s_qn = reinterpret_cast<T*>(smem + C::QN_OFF);
+    for (int h = warp; h < G; h += kNW) {
+      const T* qrow = static_cast<const T*>(a.q) + (static_cast<size_t>(bt) * a.H + kvh * G + h) * HD;
+      float f[C::EL];
+      load_row<T, C::NPC, C::PE>(qrow, lane, f);
+      norm_rope_row<T, HD, C::NPC, C::PE>(f, a.q_w, true, s_cos, s_sin, a.n_rot, a.eps, lane);
+      store_row<T, C::NPC, C::PE>(s_qn + h * HD, lane, f);
+    }
+    __syncthreads();
   }
 
   // q of the G heads, pre-scaled into the log2 domain.
   float2 q2[G][EL2];
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    const T* qrow = static_cast<const T*>(a.q) + (static_cast<size_t>(bt) * a.H + kvh * G + h) * HD;
+    const T* qrow = FUSED ? reinterpret_cast<const T*>(smem + C::QN_OFF) + h * HD
+                          : static_cast<const T*>(a.q) + (static_cast<size_t>(bt) * a.H + kvh * G + h) * HD;
     float f[C::EL];
     load_row<T, C::NPC, C::PE>(qrow, lane, f);
-    if constexpr (FUSED) norm_rope_row<T, HD, C::NPC, C::PE>(f, a.q_w, true, s_cos, s_sin, a.n_rot, a.eps, lane);
 #pragma unroll
     for (int i = 0; i < C::EL; ++i) f[i] *= a.scale_log2;
     to_f2<C::EL>(f, q2[h]);

@@ -23,6 +23,7 @@ struct AppendArgs {
   void* cache_v;
   int B, T, H, Hkv, hd, max_len;
   int rows_per_cta;  // head rows (of H + 2 Hkv) handled per CTA
+  int tok_per_cta;   // tokens (same t, consecutive b) handled per CTA
   int n_rot;         // rotated pairs; inv_freq[j] == 0 for j >= n_rot
   float eps;
   float inv_freq[kMaxHalf];

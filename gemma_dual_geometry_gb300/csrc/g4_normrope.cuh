@@ -17,10 +17,10 @@
 //     rounding is the correct one (Ziv's rounding test);
 //   * otherwise a double-float evaluation decides: values carried as an
 //     unevaluated sum of two floats, built from Dekker's exact product (one
-//     fma) and Knuth's two-sum, accurate to about 2^-44 relative.
-// The row's sum of squares and inverse root, and cos / sin of every rotated
-// pair, are always kept in double-float; cos / sin come from Cody-Waite
-// reduction by a three-float pi/2 and Taylor polynomials on [-pi/4, pi/4].
+//     fma) and Knuth's two-sum, accurate to about 2^-44 relative.  It runs
+//     for well under one element in a thousand.
+// cos / sin in double-float come from an exact p * f, Cody-Waite reduction
+// by a three-float pi/2 and Taylor polynomials on [-pi/4, pi/4].
 #pragma once
 
 #include "g4_device.cuh"
@@ -90,6 +90,34 @@ __device__ __forceinline__ float bf16_midpoint(float v) {
   return __uint_as_float((__float_as_uint(v) & 0xFFFF0000u) | 0x8000u);
 }
 
+constexpr int ilog2c(int x) { return x <= 1 ? 0 : 1 + ilog2c(x / 2); }
+
+// Row sum of squares in float32: pairwise over the lane's N elements, then
+// the 32-lane butterfly (every lane ends with the same value).  Relative
+// error at most (log2 N + 5) u, u = 2^-24.
+template <int N>
+__device__ __forceinline__ float row_sumsq_f32(const float* x) {
+  float v[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] = x[i] * x[i];
+#pragma unroll
+  for (int w = N / 2; w >= 1; w /= 2)
+#pragma unroll
+    for (int i = 0; i < w; ++i) v[i] += v[i + w];
+  float s = v[0];
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s;
+}
+
+// Bound, in units of u, on the relative error of y = fl(fl(x r) w) with
+// r = rsqrt_rn(fl(S / hd + eps)) and S from row_sumsq_f32<N>: the sum, the
+// eps addition (halved by the root), the correctly rounded root, two products.
+template <int N>
+constexpr float norm_err_units() {
+  return (ilog2c(N) + 6) * 0.5f + 3.0f;
+}
+
 // Row sum of squares in double-float over the lane's n elements, then over
 // the 32 lanes of the warp (every lane ends with the same value).
 template <int N>
@@ -121,12 +149,11 @@ __device__ __forceinline__ DF inv_rms_df(DF sumsq, int hd, float eps) {
   return fast_two_sum(r0, r0 * (0.5f * d));
 }
 
-// cos and sin of p * f (p an integer position, f a float32 frequency) in
-// double-float.
-__device__ __forceinline__ void sincos_df(int p, float f, DF& c_out, DF& s_out) {
+// p * f (p an integer position, f a float32 frequency) reduced to r in
+// [-pi/4, pi/4] (+ a rounding of k) in double-float, and its quadrant k mod 4.
+__device__ __forceinline__ DF reduce_angle_df(int p, float f, int& quadrant) {
   DF r;
-  int quadrant;
-  if (p < (1 << 24)) {
+  if (p < (1 << 24) && p > -(1 << 24)) {
     // theta = p * f exactly (p is exact in float); k = nearest multiple of pi/2
     const DF th = two_prod(static_cast<float>(p), f);
     const float k = rintf(th.h * 0x1.45f306p-1f);  // 2 / pi
@@ -148,6 +175,13 @@ __device__ __forceinline__ void sincos_df(int p, float f, DF& c_out, DF& s_out) 
     r.l = static_cast<float>(rd - static_cast<double>(r.h));
     quadrant = static_cast<int>(fmod(k, 4.0) + 4.0) & 3;
   }
+  return r;
+}
+
+// cos and sin of p * f in double-float (absolute error about 2^-47).
+__device__ __forceinline__ void sincos_df(int p, float f, DF& c_out, DF& s_out) {
+  int quadrant;
+  const DF r = reduce_angle_df(p, f, quadrant);
   // Taylor polynomials on |r| <= pi/4 (+ a rounding of k): the leading
   // coefficients 1/n! in double-float, the tail (< 2^-30 of the result) in float.
   const DF z = df_mul(r, r);
@@ -177,46 +211,58 @@ __device__ __forceinline__ void sincos_df(int p, float f, DF& c_out, DF& s_out) 
   }
 }
 
-// The float32 evaluation of one output is off from the exact value by at
-// most 6u (|y_a| + |y_b|), u = 2^-24 (three roundings in y, one in cos / sin,
-// one in the product, one in the fma); the test uses twice that.
-constexpr float kNormRopeErr = 12.0f * 0x1.0p-24f;
+// Error of a double-float table's float part: at most u (+ 2^-47).
+constexpr float kDFTrigErrUnits = 1.0f;
 
 // Exact value of one output of a pair, rounded to bf16: y_self * c +- y_other
 // * s on a rotated pair (sign - for the lower element), else y_self.
 static __device__ __noinline__ float normrope_exact_bf16(float x_self, float w_self, float x_other, float w_other, DF r,
-                                                  bool rot, bool lower, DF c, DF s) {
+                                                         bool rot, bool lower, DF c, DF s) {
   const DF ys = df_mul_f(df_mul_f(r, x_self), w_self);
   if (!rot) return df_round_bf16(ys);
   const DF yo = df_mul_f(df_mul_f(r, x_other), w_other);
   return df_round_bf16(df_add(df_mul(ys, c), df_mul(yo, lower ? df_neg(s) : s)));
 }
 
-// One pair (lower a = element j, upper b = element j + hd/2) of a row whose
-// inverse rms is r.  Returns the two outputs as floats; with BF16 set they
-// are exactly the correctly rounded bf16 values, else float32 results.
-template <bool BF16>
-__device__ __forceinline__ void normrope_pair(float xa, float wa, float xb, float wb, DF r, bool rot, DF c, DF s,
-                                              float& oa, float& ob) {
-  const float ya = (xa * r.h) * wa;
-  const float yb = (xb * r.h) * wb;
+// Float32 evaluation of one pair (lower a = element j, upper b = element
+// j + hd/2) with row inverse rms r, cos / sin c, s.  Sets need_a / need_b
+// when the float32 value cannot decide the bf16 rounding; err_y and err_rot
+// are the bounds (already multiplied by u and a safety margin) for an
+// unrotated output (times |y|) and a rotated one (times |y_a| + |y_b|).
+__device__ __forceinline__ void normrope_pair_fast(float xa, float wa, float xb, float wb, float r, bool rot, float c,
+                                                   float s, float err_y, float err_rot, float& oa, float& ob,
+                                                   bool& need_a, bool& need_b) {
+  const float ya = (xa * r) * wa;
+  const float yb = (xb * r) * wb;
   float ea, eb;
   if (rot) {
-    oa = fmaf(ya, c.h, -(yb * s.h));
-    ob = fmaf(yb, c.h, ya * s.h);
-    ea = eb = kNormRopeErr * (fabsf(ya) + fabsf(yb));
+    oa = fmaf(ya, c, -(yb * s));
+    ob = fmaf(yb, c, ya * s);
+    ea = eb = err_rot * (fabsf(ya) + fabsf(yb));
   } else {
     oa = ya;
     ob = yb;
-    ea = kNormRopeErr * fabsf(ya);
-    eb = kNormRopeErr * fabsf(yb);
+    ea = err_y * fabsf(ya);
+    eb = err_y * fabsf(yb);
   }
-  if constexpr (BF16) {
-    if (fabsf(oa - bf16_midpoint(oa)) > ea) oa = __bfloat162float(__float2bfloat16_rn(oa));
-    else oa = normrope_exact_bf16(xa, wa, xb, wb, r, rot, true, c, s);
-    if (fabsf(ob - bf16_midpoint(ob)) > eb) ob = __bfloat162float(__float2bfloat16_rn(ob));
-    else ob = normrope_exact_bf16(xb, wb, xa, wa, r, rot, false, c, s);
-  }
+  need_a = !(fabsf(oa - bf16_midpoint(oa)) > ea);
+  need_b = !(fabsf(ob - bf16_midpoint(ob)) > eb);
+}
+
+// Bounds for normrope_pair_fast with N elements per lane, the cos / sin error
+// trig_units, and a 1.5x margin.
+template <int N>
+constexpr float normrope_err_y() {
+  return 1.5f * norm_err_units<N>() * 0x1.0p-24f;
+}
+template <int N>
+constexpr float normrope_err_rot(float trig_units) {
+  return 1.5f * (norm_err_units<N>() + trig_units + 2.0f) * 0x1.0p-24f;
+}
+
+// Inverse rms of a row in float32 (all lanes), from row_sumsq_f32.
+__device__ __forceinline__ float inv_rms_f32(float sumsq, int hd, float eps) {
+  return __frsqrt_rn(fmaf(sumsq, 1.0f / static_cast<float>(hd), eps));
 }
 
 }  // namespace g4
