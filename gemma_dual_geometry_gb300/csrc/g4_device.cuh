@@ -17,6 +17,7 @@ namespace g4 {
 
 // Device error word codes (the word itself lives in g4_api.cu).
 constexpr int kErrWaitTimeout = 1;
+constexpr int kErrSmemAlign = 2;
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
@@ -194,6 +195,23 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* er
   }
 }
 
+// Single-thread bounded wait, for a warp role whose work is done by one
+// elected lane (the TMA producer, the MMA issuer): same limits and error
+// reporting as warp_wait.
+__device__ __forceinline__ bool thread_wait(uint32_t bar, uint32_t parity, int* err, volatile int* abort = nullptr) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    const bool aborted = abort != nullptr && *abort;
+    if (aborted || global_ns() - t0 > kWaitLimitNs) {
+      if (!aborted && err) atomicExch(err, kErrWaitTimeout);
+      if (abort) *abort = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
 // ---------------------------------------------------------------- async copies
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -216,6 +234,15 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
       "%5}], [%6];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
       : "memory");
 }
 

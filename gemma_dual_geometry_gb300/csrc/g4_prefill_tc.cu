@@ -20,16 +20,20 @@
 //                                        TMEM, B = V_j MN-major)
 //               in the order QK_0, QK_1, PV_0, QK_2, PV_1, ... so the score
 //               MMA of the next tile overlaps the softmax of this one.
-//   warps 2-5   softmax, one query row per thread (TMEM lane = row): load S
-//               with tcgen05.ld, mask (causal / window / keys past the cache),
+//   warps 2-9   softmax: two warps per TMEM lane quarter (a warp may only
+//               touch its quarter's 32 lanes), each thread half a query row
+//               (64 of the 128 score columns; TMEM lane = row): load the
+//               whole S row with tcgen05.ld (both threads of a row find the
+//               same maximum), mask (causal / window / keys past the cache),
 //               online softmax in the log2 domain with the running maximum
-//               raised only when it grows by more than 2^8 (the stale maximum
-//               is exact for O / l), rescale the O row in TMEM when it is
-//               raised, and write P as bf16 over the first 64 columns of the
-//               same S buffer; finally O / l to global memory.  The row sum
-//               l adds the bf16-rounded P values, the weights the PV MMA
-//               really applies, so a row dominated by one key returns that
-//               key's value without the rounding error of P.
+//               raised only when it grows by more than 2^64 (the stale
+//               maximum is exact for O / l), rescale its half of the O row in
+//               TMEM when it is raised, and write its P half as bf16 over the
+//               S buffer (packed: 32 columns); finally its half of O / l to
+//               global memory (the two halves' row sums meet in shared
+//               memory once, at the end).  The row sum l adds the bf16-rounded P values, the
+//               weights the PV MMA really applies, so a row dominated by one
+//               key returns that key's value without the rounding error of P.
 // TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O [256, 256 + DV).
 // The MMAs of one thread execute in issue order, so QK_{j+2} (issued after
 // PV_j) overwrites P_j only after PV_j has read it; no barrier is needed
@@ -46,28 +50,40 @@ namespace {
 
 constexpr int kBM = 128;       // query rows per CTA
 constexpr int kBN = 128;       // keys per tile
-constexpr int kSlotB = 16384;  // ring slot bytes
-constexpr int kThreads = 192;
+constexpr int kChunkB = 16384;  // 128 rows x 64 bf16, one 128-byte-swizzled block
+constexpr int kThreads = 320;  // 10 warps
 constexpr int kMaxSlots = 12;
 constexpr int kSmemMax = 232448;  // opt-in shared memory per block
-constexpr float kRescaleLog2 = 8.0f;
+// The exponent base of a row is raised only when a tile's maximum exceeds it
+// by more than 2^64: P <= 2^64 in bf16 and O <= 2^64 * keys * |v| in f32 stay
+// far from overflow, and rescaling O (a TMEM round trip) becomes rare.
+constexpr float kRescaleLog2 = 64.0f;
 
 template <int HD>
 struct TcCfg {
   static constexpr int DV = HD < 256 ? HD : 256;  // output columns per CTA
   static constexpr int NDH = HD / DV;             // CTAs per (tile, head)
   static constexpr int QCH = HD / 64;             // 64-dim chunks of Q and of a K tile
-  static constexpr int VK = 8192 / DV;            // keys per V chunk (VK * DV * 2 = 16 KB)
-  static constexpr int VCH = kBN / VK;            // V chunks per tile
+  // A TMA request costs the SM about 576 cycles whatever its size up to
+  // 32 KB (64 KB: ~900), so tiles move as few large multi-dimensional boxes:
+  // a K part is 128 keys x CPP 64-dim chunks, a V part VKP keys x DV dims.
+  static constexpr int KPARTS = HD == 512 ? 4 : 1;
+  static constexpr int CPP = QCH / KPARTS;          // 64-dim chunks per K part
+  static constexpr int KPB = CPP * kChunkB;         // K part bytes
+  static constexpr int VKP = HD == 512 ? 64 : 128;  // keys per V part
+  static constexpr int VPARTS = kBN / VKP;
+  static constexpr int VPB = VKP * DV * 2;          // V part bytes
+  static constexpr int SLOTB = KPB > VPB ? KPB : VPB;
   static constexpr int Q_OFF = 0;
-  static constexpr int RING_OFF = Q_OFF + QCH * kSlotB;
-  static constexpr int BAR_B = 512;
-  static constexpr int NSLOT_FIT = (kSmemMax - 1024 - BAR_B - RING_OFF) / kSlotB;
+  static constexpr int RING_OFF = Q_OFF + QCH * kChunkB;
+  static constexpr int BAR_B = 3072;
+  static constexpr int NSLOT_FIT = (kSmemMax - BAR_B - RING_OFF) / SLOTB;
   static constexpr int NSLOT = NSLOT_FIT < kMaxSlots ? NSLOT_FIT : kMaxSlots;
-  static constexpr int BAR_OFF = RING_OFF + NSLOT * kSlotB;
-  static constexpr int SMEM_B = 1024 + BAR_OFF + BAR_B;  // + alignment slack
-  static_assert(NSLOT >= 4, "ring depth");
+  static constexpr int BAR_OFF = RING_OFF + NSLOT * SLOTB;
+  static constexpr int SMEM_B = BAR_OFF + BAR_B;
+  static_assert(NSLOT >= 2, "ring depth");
   static_assert(SMEM_B <= kSmemMax, "shared memory budget");
+  static_assert(VKP % 16 == 0 && kBN % VKP == 0 && QCH % KPARTS == 0, "tiling");
 };
 
 struct TcBars {
@@ -76,20 +92,27 @@ struct TcBars {
   uint64_t p_full[2];  // P_j written to TMEM by all 128 softmax threads
   uint64_t o_done[2];  // PV_j complete
   uint64_t drain;
+  uint64_t sum_full[4];  // [lane quarter]: both row-sum shares written
   uint64_t full[kMaxSlots];
   uint64_t empty[kMaxSlots];
   uint32_t tmem_base;
   int abort;
+  float red[2][kBM];  // [column half][row]: row-sum shares
 };
-static_assert(sizeof(TcBars) <= 512, "barrier block");
+static_assert(sizeof(TcBars) <= 3072, "barrier block");
 
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ PrefillTcArgs a) {
   using C = TcCfg<HD>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 128-byte-swizzled tiles need 1024-byte alignment; the declaration asks
+  // for it, and a block that does not get it reports and does nothing.
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicExch(a.err, kErrSmemAlign);
+    return;
+  }
   TcBars* bars = reinterpret_cast<TcBars*>(smem + C::BAR_OFF);
   const uint32_t sQ = smem_u32(smem + C::Q_OFF);
   const uint32_t sRing = smem_u32(smem + C::RING_OFF);
@@ -126,14 +149,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(smem_u32(&bars->q_full), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->s_full[i]), 1);
-      mbar_init(smem_u32(&bars->p_full[i]), 128);
+      mbar_init(smem_u32(&bars->p_full[i]), 256);
       mbar_init(smem_u32(&bars->o_done[i]), 1);
     }
     mbar_init(smem_u32(&bars->drain), 1);
-    for (int i = 0; i < C::NSLOT; ++i) {
-      mbar_init(smem_u32(&bars->full[i]), 1);
-      mbar_init(smem_u32(&bars->empty[i]), 1);
-    }
+    for (int qq = 0; qq < 4; ++qq) mbar_init(smem_u32(&bars->sum_full[qq]), 64);
+    for (int i = 0; i < C::NSLOT; ++i) mbar_init(smem_u32(&bars->full[i]), 1);
+    for (int i = 0; i < C::NSLOT; ++i) mbar_init(smem_u32(&bars->empty[i]), 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -149,130 +171,149 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int seq = 0;
+    // One lane issues every copy (a warp-wide wait per slot would cost more
+    // than the copy takes to issue).
     if (lane == 0 && ntiles > 0) {
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
       const uint32_t qb = smem_u32(&bars->q_full);
-      mbar_arrive_expect_tx(qb, C::QCH * kSlotB);
-      for (int c = 0; c < C::QCH; ++c) tma_load_4d(sQ + c * kSlotB, &tm_q, c * 64, h, q0, b, qb);
-    }
-    bool ok = true;
-    auto acquire = [&](int& slot) -> bool {
-      slot = seq % C::NSLOT;
-      const uint32_t par = ((seq / C::NSLOT) & 1) ^ 1;
-      return warp_wait(smem_u32(&bars->empty[slot]), par, a.err, abort);
-    };
-    auto load_k = [&](int kt) {
-      for (int c = 0; c < C::QCH && ok; ++c) {
-        int slot;
-        if (!acquire(slot)) { ok = false; break; }
-        if (lane == 0) {
-          const uint32_t fb = smem_u32(&bars->full[slot]);
-          mbar_arrive_expect_tx(fb, kSlotB);
-          tma_load_4d(sRing + slot * kSlotB, &tm_k, c * 64, kt * kBN, kvh, b, fb);
-        }
-        __syncwarp();
+      mbar_arrive_expect_tx(qb, C::QCH * kChunkB);
+      // Q tile: 128 rows x QCH chunks in one request (two for head_dim 512)
+      constexpr int QREQ = C::QCH > 4 ? 2 : 1;
+#pragma unroll
+      for (int r = 0; r < QREQ; ++r)
+        tma_load_5d(sQ + r * (C::QCH / QREQ) * kChunkB, &tm_q, 0, q0, r * (C::QCH / QREQ), h, b, qb);
+      bool ok = true;
+      int seq = 0;
+      int slot = 0;        // ring slot of the next part
+      uint32_t phase = 0;  // parity of that slot's current use
+      auto advance = [&]() {
         ++seq;
-      }
-    };
-    auto load_v = [&](int kt) {
-      for (int c = 0; c < C::VCH && ok; ++c) {
-        int slot;
-        if (!acquire(slot)) { ok = false; break; }
-        if (lane == 0) {
-          const uint32_t fb = smem_u32(&bars->full[slot]);
-          mbar_arrive_expect_tx(fb, kSlotB);
-          for (int dc = 0; dc < C::DV / 64; ++dc)
-            tma_load_4d(sRing + slot * kSlotB + dc * C::VK * 128, &tm_v, dh * C::DV + dc * 64,
-                        kt * kBN + c * C::VK, kvh, b, fb);
+        if (++slot == C::NSLOT) {
+          slot = 0;
+          phase ^= 1u;
         }
-        __syncwarp();
-        ++seq;
-      }
-    };
-    if (ntiles > 0) {
+      };
+      auto load_k = [&](int kt) {
+        for (int p2 = 0; p2 < C::KPARTS && ok; ++p2) {
+          if (!thread_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, a.err, abort)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&bars->full[slot]);
+          mbar_arrive_expect_tx(fb, C::KPB);
+          tma_load_5d(sRing + slot * C::SLOTB, &tm_k, 0, kt * kBN, p2 * C::CPP, kvh, b, fb);
+          advance();
+        }
+      };
+      auto load_v = [&](int kt) {
+        for (int p2 = 0; p2 < C::VPARTS && ok; ++p2) {
+          if (!thread_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, a.err, abort)) { ok = false; break; }
+          const uint32_t fb = smem_u32(&bars->full[slot]);
+          mbar_arrive_expect_tx(fb, C::VPB);
+          tma_load_5d(sRing + slot * C::SLOTB, &tm_v, 0, kt * kBN + p2 * C::VKP, dh * (C::DV / 64), kvh, b, fb);
+          advance();
+        }
+      };
       load_k(kt_begin);
       for (int j = 0; j < ntiles && ok; ++j) {
         if (j + 1 < ntiles) load_k(kt_begin + j + 1);
         load_v(kt_begin + j);
       }
       // Copies still in flight must land before the CTA may exit.
-      warp_wait(smem_u32(&bars->q_full), 0, nullptr);
-      for (int s = max(0, seq - C::NSLOT); s < seq; ++s)
-        warp_wait(smem_u32(&bars->full[s % C::NSLOT]), (s / C::NSLOT) & 1, nullptr);
+      thread_wait(smem_u32(&bars->q_full), 0, nullptr);
+      for (int s2 = max(0, seq - C::NSLOT); s2 < seq; ++s2)
+        thread_wait(smem_u32(&bars->full[s2 % C::NSLOT]), (s2 / C::NSLOT) & 1, nullptr);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (ntiles > 0) {
+    // One lane waits and issues (tcgen05.mma is issued by a single thread;
+    // waiting with the whole warp only adds latency between MMAs).
+    if (lane == 0 && ntiles > 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, C::DV, 0, 1);
-      int seq = 0;
-      bool ok = warp_wait(smem_u32(&bars->q_full), 0, a.err, abort);
+      bool ok = thread_wait(smem_u32(&bars->q_full), 0, a.err, abort);
       tc_fence_after();
+      // Descriptors are built once; a slot, a 64-dim chunk or a 16-element
+      // K step only moves the start address (16-byte units in the low bits,
+      // which stay below 2^14 for any shared-memory address).  Building them
+      // per instruction costs the issuing thread more cycles than the MMA.
+      const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(sRing, 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(sRing, C::VKP * 128, 1024);
+      // Ring state, advanced incrementally: the issuing thread's own
+      // instruction latency sits between MMAs of 64 cycles, so there is no
+      // division, modulo or multiply on this path.
+      int slot = 0;        // ring slot of the next part
+      uint32_t phase = 0;  // parity of that slot's current use
+      uint32_t soff = 0;   // slot * SLOTB in descriptor units (16 bytes)
+      const uint32_t full0 = smem_u32(&bars->full[0]);
+      const uint32_t empty0 = smem_u32(&bars->empty[0]);
+      auto release = [&]() {
+        tc_commit(empty0 + slot * 8);
+        soff += C::SLOTB >> 4;
+        if (++slot == C::NSLOT) {
+          slot = 0;
+          phase ^= 1u;
+          soff = 0;
+        }
+      };
       auto mma_qk = [&](int j) {
         const int sb = j & 1;
         const uint32_t dS = tmem + sb * kBN;
-        for (int c = 0; c < C::QCH; ++c) {
-          const int slot = seq % C::NSLOT;
-          if (!warp_wait(smem_u32(&bars->full[slot]), (seq / C::NSLOT) & 1, a.err, abort)) { ok = false; return; }
+        uint64_t ad = dq0;
+#pragma unroll 1
+        for (int p2 = 0; p2 < C::KPARTS; ++p2) {
+          if (!thread_wait(full0 + slot * 8, phase, a.err, abort)) { ok = false; return; }
           tc_fence_after();
-          if (lane == 0) {
+          uint64_t bd = dk0 + soff;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t ad = smem_desc_sw128(sQ + c * kSlotB + kk * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(sRing + slot * kSlotB + kk * 32, 16, 1024);
-              tc_mma_ss(dS, ad, bd, idesc_qk, (c > 0 || kk > 0) ? 1u : 0u);
-            }
-            tc_commit(smem_u32(&bars->empty[slot]));
+          for (int c = 0; c < C::CPP; ++c) {
+            tc_mma_ss(dS, ad, bd, idesc_qk, (p2 > 0 || c > 0) ? 1u : 0u);
+            tc_mma_ss(dS, ad + 2, bd + 2, idesc_qk, 1u);
+            tc_mma_ss(dS, ad + 4, bd + 4, idesc_qk, 1u);
+            tc_mma_ss(dS, ad + 6, bd + 6, idesc_qk, 1u);
+            ad += kChunkB >> 4;
+            bd += kChunkB >> 4;
           }
-          __syncwarp();
-          ++seq;
+          release();
         }
-        if (lane == 0) tc_commit(smem_u32(&bars->s_full[sb]));
-        __syncwarp();
+        tc_commit(smem_u32(&bars->s_full[sb]));
       };
       auto mma_pv = [&](int j) {
         const int sb = j & 1;
-        if (!warp_wait(smem_u32(&bars->p_full[sb]), (j >> 1) & 1, a.err, abort)) { ok = false; return; }
+        if (!thread_wait(smem_u32(&bars->p_full[sb]), (j >> 1) & 1, a.err, abort)) { ok = false; return; }
         tc_fence_after();
         const int kt = kt_begin + j;
-        const uint32_t tP = tmem + sb * kBN;  // P_j: 128 keys as 64 packed columns
-        for (int c = 0; c < C::VCH; ++c) {
-          const int slot = seq % C::NSLOT;
-          if (!warp_wait(smem_u32(&bars->full[slot]), (seq / C::NSLOT) & 1, a.err, abort)) { ok = false; return; }
+        uint32_t ta = tmem + sb * kBN;  // P_j: 128 keys as 64 packed columns
+#pragma unroll 1
+        for (int p2 = 0; p2 < C::VPARTS; ++p2) {
+          if (!thread_wait(full0 + slot * 8, phase, a.err, abort)) { ok = false; return; }
           // Rows of keys past the cache's filled length may hold anything
-          // (even NaN, and 0 * NaN = NaN); zero them before they meet P.
-          const int key0 = kt * kBN + c * C::VK;
-          const int nvalid = min(C::VK, max(0, Lk - key0));
-          if (nvalid < C::VK) {
-            uint8_t* slot_ptr = smem + C::RING_OFF + slot * kSlotB;
-            const int nbad = C::VK - nvalid;
-            for (int i = lane; i < (C::DV / 64) * nbad * 8; i += 32) {
+          // (even NaN, and 0 * NaN = NaN); zero them before they meet P
+          // (only in the part holding the end of the keys).
+          const int key0 = kt * kBN + p2 * C::VKP;
+          if (key0 + C::VKP > Lk) {
+            const int nvalid = max(0, Lk - key0);
+            uint8_t* slot_ptr = smem + C::RING_OFF + slot * C::SLOTB;
+            const int nbad = C::VKP - nvalid;
+            for (int i = 0; i < (C::DV / 64) * nbad * 8; ++i) {
               const int dc = i / (nbad * 8);
               const int rr = (i / 8) % nbad + nvalid;
               const int pc = i % 8;
-              *reinterpret_cast<uint4*>(slot_ptr + dc * C::VK * 128 + rr * 128 + pc * 16) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(slot_ptr + dc * C::VKP * 128 + rr * 128 + pc * 16) = make_uint4(0, 0, 0, 0);
             }
             fence_proxy_async_smem();
-            __syncwarp();
           }
           tc_fence_after();
-          if (lane == 0) {
+          const uint64_t bd = dv0 + soff;
 #pragma unroll
-            for (int kk = 0; kk < C::VK / 16; ++kk) {
-              const int kp = c * C::VK + kk * 16;  // key offset inside the tile
-              const uint64_t bd = smem_desc_sw128(sRing + slot * kSlotB + kk * 2048, C::VK * 128, 1024);
-              tc_mma_ts(tmem_O, tP + kp / 2, bd, idesc_pv, (j > 0 || c > 0 || kk > 0) ? 1u : 0u);
-            }
-            tc_commit(smem_u32(&bars->empty[slot]));
-          }
-          __syncwarp();
-          ++seq;
+          for (int kk = 0; kk < C::VKP / 16; ++kk)
+            tc_mma_ts(tmem_O, ta + kk * 8, bd + static_cast<uint64_t>(kk * 128), idesc_pv,
+                      (j > 0 || p2 > 0 || kk > 0) ? 1u : 0u);
+          ta += C::VKP / 2;
+          release();
         }
-        if (lane == 0) tc_commit(smem_u32(&bars->o_done[sb]));
-        __syncwarp();
+        tc_commit(smem_u32(&bars->o_done[sb]));
       };
       if (ok) mma_qk(0);
       for (int j = 0; j < ntiles && ok; ++j) {
@@ -280,58 +321,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) mma_pv(j);
       }
       // Every MMA issued so far completes before TMEM is released.
-      if (lane == 0) tc_commit(smem_u32(&bars->drain));
-      __syncwarp();
-      warp_wait(smem_u32(&bars->drain), 0, nullptr);
+      tc_commit(smem_u32(&bars->drain));
+      thread_wait(smem_u32(&bars->drain), 0, nullptr);
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
     const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;  // which 64 of the 128 score columns
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int qpos = qpos_first + r;
     const bool row_valid = r < valid_rows;
     const float c2 = a.scale_log2;  // > 0 (checked on the host)
+    constexpr int kHB = kBN / 2;    // score columns per thread
+    constexpr int kDVH = C::DV / 2; // O columns per thread
     float m = -INFINITY;  // exponent base in log2 units: a stale running maximum
-    float l = 0.0f;
+    float l = 0.0f;       // this half's share of the row sum
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
       const int sb = j & 1;
       if (!warp_wait(smem_u32(&bars->s_full[sb]), (j >> 1) & 1, a.err, abort)) { ok = false; break; }
       tc_fence_after();
-      float s[kBN];
+      float s[kHB];
+      float mt;
       {
-        uint32_t r0[32], r1[32], r2[32], r3[32];
+        // the whole row: both threads of a row take the same maximum
+        uint32_t r0[32], r1[32], o0[32], o1[32];
         const uint32_t tS = tmem + lane_off + sb * kBN;
-        tmem_ld32(tS, r0);
-        tmem_ld32(tS + 32, r1);
-        tmem_ld32(tS + 64, r2);
-        tmem_ld32(tS + 96, r3);
+        tmem_ld32(tS + half * kHB, r0);
+        tmem_ld32(tS + half * kHB + 32, r1);
+        tmem_ld32(tS + (1 - half) * kHB, o0);
+        tmem_ld32(tS + (1 - half) * kHB + 32, o1);
         tc_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           s[i] = __uint_as_float(r0[i]);
           s[32 + i] = __uint_as_float(r1[i]);
-          s[64 + i] = __uint_as_float(r2[i]);
-          s[96 + i] = __uint_as_float(r3[i]);
         }
-      }
-
-      const int k0 = (kt_begin + j) * kBN;
-      const bool all_vis = row_valid && (k0 + kBN - 1 <= qpos) && (k0 + kBN <= Lk) &&
-                           (!a.sliding || qpos - k0 < a.window);
-      if (!all_vis) {
+        const int kr = (kt_begin + j) * kBN;
+        const bool row_vis = row_valid && (kr + kBN - 1 <= qpos) && (kr + kBN <= Lk) &&
+                             (!a.sliding || qpos - kr < a.window);
+        const int k0 = kr + half * kHB;
+        const int k1 = kr + (1 - half) * kHB;
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (row_vis) {
 #pragma unroll
-        for (int n = 0; n < kBN; ++n) {
-          const int kp = k0 + n;
-          const bool vis = row_valid && kp <= qpos && kp < Lk && (!a.sliding || qpos - kp < a.window);
-          if (!vis) s[n] = -INFINITY;
+          for (int n = 0; n < 32; ++n) {
+            mx[n & 3] = fmaxf(mx[n & 3], fmaxf(s[n], s[32 + n]));
+            mx[(n + 2) & 3] = fmaxf(mx[(n + 2) & 3], fmaxf(__uint_as_float(o0[n]), __uint_as_float(o1[n])));
+          }
+        } else {
+#pragma unroll
+          for (int n = 0; n < kHB; ++n) {
+            const int kp = k0 + n;
+            const bool vis = row_valid && kp <= qpos && kp < Lk && (!a.sliding || qpos - kp < a.window);
+            if (!vis) s[n] = -INFINITY;
+            mx[n & 3] = fmaxf(mx[n & 3], s[n]);
+          }
+#pragma unroll
+          for (int n = 0; n < 32; ++n) {
+            const int kp0 = k1 + n, kp1 = k1 + 32 + n;
+            const bool v0 = row_valid && kp0 <= qpos && kp0 < Lk && (!a.sliding || qpos - kp0 < a.window);
+            const bool v1 = row_valid && kp1 <= qpos && kp1 < Lk && (!a.sliding || qpos - kp1 < a.window);
+            if (v0) mx[n & 3] = fmaxf(mx[n & 3], __uint_as_float(o0[n]));
+            if (v1) mx[(n + 1) & 3] = fmaxf(mx[(n + 1) & 3], __uint_as_float(o1[n]));
+          }
         }
+        mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
       }
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int n = 0; n < kBN; ++n) mx[n & 3] = fmaxf(mx[n & 3], s[n]);
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
       float alpha = 1.0f;
       bool rescale = false;
       float m_use = m;
@@ -353,33 +411,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const float f = rescale ? alpha : 1.0f;
 #pragma unroll 1
-        for (int cc = 0; cc < C::DV / 32; ++cc) {
+        for (int cc = 0; cc < kDVH / 32; ++cc) {
           uint32_t rr[32];
-          tmem_ld32(tmem_O + lane_off + cc * 32, rr);
+          const uint32_t tO = tmem_O + lane_off + half * kDVH + cc * 32;
+          tmem_ld32(tO, rr);
           tc_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * f);
-          tmem_st32(tmem_O + lane_off + cc * 32, rr);
+          tmem_st32(tO, rr);
         }
         tc_wait_st();
       }
       const float nb = (m_use == -INFINITY) ? 0.0f : -m_use;
-      uint32_t p0[32], p1[32];
+      uint32_t p[32];
       float sa[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const uint32_t w0 = pack_bf16x2(ex2_approx(fmaf(s[2 * i], c2, nb)), ex2_approx(fmaf(s[2 * i + 1], c2, nb)));
-        const uint32_t w1 =
-            pack_bf16x2(ex2_approx(fmaf(s[64 + 2 * i], c2, nb)), ex2_approx(fmaf(s[64 + 2 * i + 1], c2, nb)));
-        p0[i] = w0;
-        p1[i] = w1;
-        sa[0] += bf16_lo(w0);
-        sa[1] += bf16_hi(w0);
-        sa[2] += bf16_lo(w1);
-        sa[3] += bf16_hi(w1);
+        const uint32_t w = pack_bf16x2(ex2_approx(fmaf(s[2 * i], c2, nb)), ex2_approx(fmaf(s[2 * i + 1], c2, nb)));
+        p[i] = w;
+        sa[(2 * i) & 3] += bf16_lo(w);
+        sa[(2 * i + 1) & 3] += bf16_hi(w);
       }
-      tmem_st32(tmem + lane_off + sb * kBN, p0);
-      tmem_st32(tmem + lane_off + sb * kBN + 32, p1);
+      tmem_st32(tmem + lane_off + sb * kBN + half * (kHB / 2), p);
       l = l * alpha + ((sa[0] + sa[1]) + (sa[2] + sa[3]));
       m = m_use;
       tc_wait_st();
@@ -387,16 +440,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(smem_u32(&bars->p_full[sb]));
     }
     if (ntiles > 0 && ok) {
+      // the full row sum: both halves' shares
+      bars->red[half][r] = l;
+      mbar_arrive(smem_u32(&bars->sum_full[quarter]));
+      ok = warp_wait(smem_u32(&bars->sum_full[quarter]), 0, a.err, abort);
+      l = bars->red[0][r] + bars->red[1][r];
+    }
+    if (ntiles > 0 && ok) {
       const int jl = ntiles - 1;
       if (warp_wait(smem_u32(&bars->o_done[jl & 1]), (jl >> 1) & 1, a.err, abort)) {
         tc_fence_after();
         const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
         __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
-                             (((static_cast<size_t>(b) * a.T + q0 + r) * a.H + h) * HD + dh * C::DV);
+                             (((static_cast<size_t>(b) * a.T + q0 + r) * a.H + h) * HD + dh * C::DV + half * kDVH);
 #pragma unroll 1
-        for (int cc = 0; cc < C::DV / 32; ++cc) {
+        for (int cc = 0; cc < kDVH / 32; ++cc) {
           uint32_t rr[32];
-          tmem_ld32(tmem_O + lane_off + cc * 32, rr);
+          tmem_ld32(tmem_O + lane_off + half * kDVH + cc * 32, rr);
           tc_wait_ld();
           if (row_valid) {
 #pragma unroll
@@ -414,8 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (ntiles == 0 && r < valid_rows) {
       // No visible key (only reachable with out-of-contract positions).
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
-                           (((static_cast<size_t>(b) * a.T + q0 + r) * a.H + h) * HD + dh * C::DV);
-      for (int i = 0; i < C::DV / 8; ++i) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
+                           (((static_cast<size_t>(b) * a.T + q0 + r) * a.H + h) * HD + dh * C::DV + half * kDVH);
+      for (int i = 0; i < kDVH / 8; ++i) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
     }
   }
 
@@ -444,13 +504,17 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// bf16 4-D tensor map, dims innermost first, 128-byte swizzle, zero fill out of bounds.
-bool make_map(CUtensorMap* m, const void* base, const cuuint64_t dims[4], const cuuint64_t strides_bytes[3],
-              const cuuint32_t box[4]) {
+// bf16 5-D tensor map, dims innermost first, 128-byte swizzle, zero fill out
+// of bounds.  Dim 0 is 64 consecutive elements (one 128-byte row), dim 1 the
+// rows (tokens or keys), dim 2 the 64-element chunks of a head, so a box of
+// (64, rows, chunks) lands in shared memory as chunk-major 128-byte rows:
+// the layout the MMA descriptors read.
+bool make_map(CUtensorMap* m, const void* base, const cuuint64_t dims[5], const cuuint64_t strides_bytes[4],
+              const cuuint32_t box[5]) {
   EncodeTiledFn fn = get_encode_fn();
   if (fn == nullptr) return false;
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides_bytes, box,
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides_bytes, box,
                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -468,19 +532,22 @@ cudaError_t launch_hd(const PrefillTcArgs& a, cudaStream_t s) {
   }
   CUtensorMap mq, mk, mv;
   const cuuint64_t row_b = static_cast<cuuint64_t>(HD) * 2;
+  constexpr cuuint32_t kQBoxChunks = C::QCH > 4 ? C::QCH / 2 : C::QCH;
   {
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(a.H),
-                                static_cast<cuuint64_t>(a.T), static_cast<cuuint64_t>(a.B)};
-    const cuuint64_t str[3] = {row_b, row_b * a.H, row_b * a.H * a.T};
-    const cuuint32_t box[4] = {64, 1, kBM, 1};
+    // q [B][T][H][hd]: (element, token, chunk, head, sequence)
+    const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(a.T), static_cast<cuuint64_t>(C::QCH),
+                                static_cast<cuuint64_t>(a.H), static_cast<cuuint64_t>(a.B)};
+    const cuuint64_t str[4] = {row_b * a.H, 128, row_b, row_b * a.H * a.T};
+    const cuuint32_t box[5] = {64, kBM, kQBoxChunks, 1, 1};
     if (!make_map(&mq, a.q, dims, str, box)) return cudaErrorInvalidValue;
   }
   {
-    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(a.max_len),
+    // cache [B][Hkv][max_len][hd]: (element, key, chunk, kv head, sequence)
+    const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(a.max_len), static_cast<cuuint64_t>(C::QCH),
                                 static_cast<cuuint64_t>(a.Hkv), static_cast<cuuint64_t>(a.B)};
-    const cuuint64_t str[3] = {row_b, row_b * a.max_len, row_b * a.max_len * a.Hkv};
-    const cuuint32_t boxk[4] = {64, kBN, 1, 1};
-    const cuuint32_t boxv[4] = {64, static_cast<cuuint32_t>(C::VK), 1, 1};
+    const cuuint64_t str[4] = {row_b, 128, row_b * a.max_len, row_b * a.max_len * a.Hkv};
+    const cuuint32_t boxk[5] = {64, kBN, C::CPP, 1, 1};
+    const cuuint32_t boxv[5] = {64, C::VKP, C::DV / 64, 1, 1};
     if (!make_map(&mk, a.ck, dims, str, boxk)) return cudaErrorInvalidValue;
     if (!make_map(&mv, a.cv, dims, str, boxv)) return cudaErrorInvalidValue;
   }

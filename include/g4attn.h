@@ -252,8 +252,10 @@ const char* g4_last_error(void);
 
 /*
  * Reads and clears the device-side error word (synchronises the device).
- * Nonzero means a kernel gave up a bounded wait (code 1) and returned early;
- * its outputs are then unspecified.  Returns -1 if the read itself failed.
+ * Nonzero means a kernel gave up a bounded wait (code 1), or found its
+ * shared memory not 1024-byte aligned (code 2, the tensor-core prefill needs
+ * that for its swizzled tiles), and returned early; its outputs are then
+ * unspecified.  Returns -1 if the read itself failed.
  */
 int32_t g4_take_device_error(void);
 
