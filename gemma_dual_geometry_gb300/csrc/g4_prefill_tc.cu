@@ -372,20 +372,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             mx[(n + 2) & 3] = fmaxf(mx[(n + 2) & 3], fmaxf(__uint_as_float(o0[n]), __uint_as_float(o1[n])));
           }
         } else {
+          // The row's visible keys are one interval [vlo, vhi): causal end,
+          // the cache's filled length and (sliding) the window start.
+          const int vlo = a.sliding ? max(0, qpos - a.window + 1) : 0;
+          const int vhi = row_valid ? min(qpos + 1, Lk) : 0;
+          const unsigned span = static_cast<unsigned>(max(0, vhi - vlo));
+          const int lo0 = vlo - k0, lo1 = vlo - k1;
 #pragma unroll
           for (int n = 0; n < kHB; ++n) {
-            const int kp = k0 + n;
-            const bool vis = row_valid && kp <= qpos && kp < Lk && (!a.sliding || qpos - kp < a.window);
-            if (!vis) s[n] = -INFINITY;
+            if (static_cast<unsigned>(n - lo0) >= span) s[n] = -INFINITY;
             mx[n & 3] = fmaxf(mx[n & 3], s[n]);
           }
 #pragma unroll
           for (int n = 0; n < 32; ++n) {
-            const int kp0 = k1 + n, kp1 = k1 + 32 + n;
-            const bool v0 = row_valid && kp0 <= qpos && kp0 < Lk && (!a.sliding || qpos - kp0 < a.window);
-            const bool v1 = row_valid && kp1 <= qpos && kp1 < Lk && (!a.sliding || qpos - kp1 < a.window);
-            if (v0) mx[n & 3] = fmaxf(mx[n & 3], __uint_as_float(o0[n]));
-            if (v1) mx[(n + 1) & 3] = fmaxf(mx[(n + 1) & 3], __uint_as_float(o1[n]));
+            const float v0 = static_cast<unsigned>(n - lo1) < span ? __uint_as_float(o0[n]) : -INFINITY;
+            const float v1 = static_cast<unsigned>(n + 32 - lo1) < span ? __uint_as_float(o1[n]) : -INFINITY;
+            mx[n & 3] = fmaxf(mx[n & 3], fmaxf(v0, v1));
           }
         }
         mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
