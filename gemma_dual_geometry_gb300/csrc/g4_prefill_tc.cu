@@ -104,7 +104,8 @@ static_assert(sizeof(TcBars) <= 3072, "barrier block");
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ PrefillTcArgs a) {
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                      const __grid_constant__ PrefillTcArgs a) {
   using C = TcCfg<HD>;
   // 128-byte-swizzled tiles need 1024-byte alignment; the declaration asks
   // for it, and a block that does not get it reports and does nothing.
@@ -448,36 +449,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_wait(smem_u32(&bars->sum_full[quarter]), 0, a.err, abort);
       l = bars->red[0][r] + bars->red[1][r];
     }
+    // Epilogue: O / l as bf16 into shared memory (the Q area: every MMA has
+    // completed once the last PV has), in the chunk-major 128-byte-swizzled
+    // layout of the output tensor map, then one TMA store of the tile.  Rows
+    // past T fall outside the map and are not written.
     if (ntiles > 0 && ok) {
       const int jl = ntiles - 1;
       if (warp_wait(smem_u32(&bars->o_done[jl & 1]), (jl >> 1) & 1, a.err, abort)) {
         tc_fence_after();
         const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
-                             (((static_cast<size_t>(b) * a.T + q0 + r) * a.H + h) * HD + dh * C::DV + half * kDVH);
-#pragma unroll 1
-        for (int cc = 0; cc < kDVH / 32; ++cc) {
-          uint32_t rr[32];
-          tmem_ld32(tmem_O + lane_off + half * kDVH + cc * 32, rr);
-          tc_wait_ld();
-          if (row_valid) {
+        constexpr int NCC = kDVH / 32;
+        uint32_t rr[NCC][32];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(rr[8 * i + 0]) * inv_l, __uint_as_float(rr[8 * i + 1]) * inv_l);
-              v.y = pack_bf16x2(__uint_as_float(rr[8 * i + 2]) * inv_l, __uint_as_float(rr[8 * i + 3]) * inv_l);
-              v.z = pack_bf16x2(__uint_as_float(rr[8 * i + 4]) * inv_l, __uint_as_float(rr[8 * i + 5]) * inv_l);
-              v.w = pack_bf16x2(__uint_as_float(rr[8 * i + 6]) * inv_l, __uint_as_float(rr[8 * i + 7]) * inv_l);
-              reinterpret_cast<uint4*>(dst + cc * 32)[i] = v;
-            }
+        for (int cc = 0; cc < NCC; ++cc) tmem_ld32(tmem_O + lane_off + half * kDVH + cc * 32, rr[cc]);
+        tc_wait_ld();
+#pragma unroll
+        for (int cc = 0; cc < NCC; ++cc) {
+          // 32 columns = half a 64-column chunk: pieces (16 bytes) p0 .. p0 + 3
+          const int col = half * kDVH + cc * 32;
+          const uint32_t row_addr = sQ + (col / 64) * kChunkB + r * 128;
+          const int p0 = (col % 64) / 8;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t x = pack_bf16x2(__uint_as_float(rr[cc][8 * i + 0]) * inv_l, __uint_as_float(rr[cc][8 * i + 1]) * inv_l);
+            const uint32_t y = pack_bf16x2(__uint_as_float(rr[cc][8 * i + 2]) * inv_l, __uint_as_float(rr[cc][8 * i + 3]) * inv_l);
+            const uint32_t z = pack_bf16x2(__uint_as_float(rr[cc][8 * i + 4]) * inv_l, __uint_as_float(rr[cc][8 * i + 5]) * inv_l);
+            const uint32_t w = pack_bf16x2(__uint_as_float(rr[cc][8 * i + 6]) * inv_l, __uint_as_float(rr[cc][8 * i + 7]) * inv_l);
+            const uint32_t addr = row_addr + (((p0 + i) ^ (r & 7)) * 16);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w)
+                         : "memory");
           }
         }
+        fence_proxy_async_smem();
       }
     } else if (ntiles == 0 && r < valid_rows) {
       // No visible key (only reachable with out-of-contract positions).
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
                            (((static_cast<size_t>(b) * a.T + q0 + r) * a.H + h) * HD + dh * C::DV + half * kDVH);
       for (int i = 0; i < kDVH / 8; ++i) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
+    }
+    // All 256 softmax threads meet here on every path (named barrier 1);
+    // after an abort the tile is left unwritten.
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (warp == 2 && lane == 0 && ntiles > 0 && !*abort) {
+      tma_store_5d(&tm_o, sQ, 0, q0, dh * (C::DV / 64), h, b);
+      bulk_commit_group();
+      bulk_wait_all();
     }
   }
 
@@ -532,7 +549,7 @@ cudaError_t launch_hd(const PrefillTcArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   const cuuint64_t row_b = static_cast<cuuint64_t>(HD) * 2;
   constexpr cuuint32_t kQBoxChunks = C::QCH > 4 ? C::QCH / 2 : C::QCH;
   {
@@ -553,6 +570,14 @@ cudaError_t launch_hd(const PrefillTcArgs& a, cudaStream_t s) {
     if (!make_map(&mk, a.ck, dims, str, boxk)) return cudaErrorInvalidValue;
     if (!make_map(&mv, a.cv, dims, str, boxv)) return cudaErrorInvalidValue;
   }
+  {
+    // out [B][T][H][hd], written DV columns (DV / 64 chunks) at a time
+    const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(a.T), static_cast<cuuint64_t>(C::QCH),
+                                static_cast<cuuint64_t>(a.H), static_cast<cuuint64_t>(a.B)};
+    const cuuint64_t str[4] = {row_b * a.H, 128, row_b, row_b * a.H * a.T};
+    const cuuint32_t box[5] = {64, kBM, C::DV / 64, 1, 1};
+    if (!make_map(&mo, a.out, dims, str, box)) return cudaErrorInvalidValue;
+  }
   const int nqt = (a.T + kBM - 1) / kBM;
   const long long nblk = static_cast<long long>(nqt) * a.H * a.B * C::NDH;
   cudaLaunchConfig_t cfg = {};
@@ -565,7 +590,7 @@ cudaError_t launch_hd(const PrefillTcArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD>, mq, mk, mv, a);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD>, mq, mk, mv, mo, a);
 }
 
 }  // namespace
