@@ -15,11 +15,22 @@
 // double-float) is built per distinct position from angle = pos *
 // inv_freq[j] with inv_freq a float32 table.  Pairs j >= n_rot (zero inv_freq) are left
 // unrotated, so those dims are the normed input.  bf16 stores are the
-// correctly rounded real results (g4_normrope.cuh).
+// correctly rounded real results (g4_normrope.cuh), decided in three stages:
+//   1. float32 for the whole row (packed float32x2 products), with Ziv's test
+//      of each value against its error bound; in the synthetic workloads
+//      about one row in five has a value the test leaves open;
+//   2. for those values only, lane by lane: the float32 inverse rms times the
+//      row's inner products in double-float, whose error is the inverse
+//      rms's alone; this leaves open about one row in twenty to thirty;
+//   3. the row's sum of squares in double-float (error-free splitting) and a
+//      double-float inverse rms, which decide the rest.
 //
 // Lane l of a warp owns elements [l*E, l*E + E) of the lower half and the
 // same offsets of the upper half (E = head_dim / 64), so each rotate_half
-// pair (j, j + head_dim/2) sits in one lane.
+// pair (j, j + head_dim/2) sits in one lane.  Each warp loads its next row
+// before it computes the current one.
+#include <type_traits>
+
 #include "g4_device.cuh"
 #include "g4_internal.h"
 #include "g4_normrope.cuh"
@@ -27,13 +38,111 @@
 namespace g4 {
 namespace {
 
+// The bits of a lane's E consecutive elements of one half of a head row.
+template <typename T, int E>
+struct HalfBits;
+template <int E>
+struct HalfBits<float, E> {
+  float v[E];
+};
+template <int E>
+struct HalfBits<__nv_bfloat16, E> {
+  uint32_t v[(E + 1) / 2];
+};
+
+template <int E>
+__device__ __forceinline__ void load_bits(const float* p, HalfBits<float, E>& h) {
+  load_elems<E>(p, h.v);
+}
+template <int E>
+__device__ __forceinline__ void load_bits(const __nv_bfloat16* p, HalfBits<__nv_bfloat16, E>& h) {
+  if constexpr (E == 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    h.v[0] = v.x; h.v[1] = v.y; h.v[2] = v.z; h.v[3] = v.w;
+  } else if constexpr (E == 4) {
+    const uint2 v = *reinterpret_cast<const uint2*>(p);
+    h.v[0] = v.x; h.v[1] = v.y;
+  } else if constexpr (E == 2) {
+    h.v[0] = *reinterpret_cast<const uint32_t*>(p);
+  } else {
+    h.v[0] = *reinterpret_cast<const uint16_t*>(p);
+  }
+}
+
+template <int E>
+__device__ __forceinline__ void unpack_bits(const HalfBits<float, E>& h, float* x) {
+#pragma unroll
+  for (int i = 0; i < E; ++i) x[i] = h.v[i];
+}
+template <int E>
+__device__ __forceinline__ void unpack_bits(const HalfBits<__nv_bfloat16, E>& h, float* x) {
+  if constexpr (E == 1) {
+    x[0] = bf16_lo(h.v[0]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < E / 2; ++i) {
+      x[2 * i] = bf16_lo(h.v[i]);
+      x[2 * i + 1] = bf16_hi(h.v[i]);
+    }
+  }
+}
+
+// y = (x * r) * w elementwise (w == nullptr: y = x * r), two elements per
+// packed float32x2 instruction; each product is rounded as its own float op.
+template <int E>
+__device__ __forceinline__ void scale_elems(float* y, const float* x, float r, const float* w) {
+  if constexpr (E % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < E; i += 2) {
+      float2 t = __fmul2_rn(make_float2(x[i], x[i + 1]), make_float2(r, r));
+      if (w != nullptr) t = __fmul2_rn(t, make_float2(w[i], w[i + 1]));
+      y[i] = t.x;
+      y[i + 1] = t.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; ++i) y[i] = w != nullptr ? (x[i] * r) * w[i] : x[i] * r;
+  }
+}
+
+// rotate_half on the lane's pairs: oa = ya c - yb s, ob = yb c + ya s, each
+// as one fma over one rounded product.
+template <int E>
+__device__ __forceinline__ void rotate_elems(float* oa, float* ob, const float* ya, const float* yb, const float* c,
+                                             const float* s) {
+  if constexpr (E % 2 == 0) {
+#pragma unroll
+    for (int i = 0; i < E; i += 2) {
+      const float2 a2 = make_float2(ya[i], ya[i + 1]);
+      const float2 b2 = make_float2(yb[i], yb[i + 1]);
+      const float2 c2 = make_float2(c[i], c[i + 1]);
+      const float2 ra = __ffma2_rn(a2, c2, __fmul2_rn(b2, make_float2(-s[i], -s[i + 1])));
+      const float2 rb = __ffma2_rn(b2, c2, __fmul2_rn(a2, make_float2(s[i], s[i + 1])));
+      oa[i] = ra.x; oa[i + 1] = ra.y;
+      ob[i] = rb.x; ob[i + 1] = rb.y;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      oa[i] = fmaf(ya[i], c[i], yb[i] * -s[i]);
+      ob[i] = fmaf(yb[i], c[i], ya[i] * s[i]);
+    }
+  }
+}
+
+// True when no bf16 rounding boundary lies within e of v (so v's own bf16
+// rounding is that of every value within e of it).
+__device__ __forceinline__ bool bf16_decided(float v, float e) { return fabsf(v - bf16_midpoint(v)) > e; }
+
 template <typename T, int HD>
-__global__ void __launch_bounds__(128) append_normrope_kernel(const __grid_constant__ AppendArgs a) {
+__global__ void __launch_bounds__(128, HD >= 512 ? 5 : 8) append_normrope_kernel(const __grid_constant__ AppendArgs a) {
   constexpr int HALF = HD / 2;
   constexpr int E = HD / 64;
   constexpr bool kBF16 = sizeof(T) == 2;
   constexpr float kErrY = normrope_err_y<2 * E>();
-  constexpr float kErrRot = normrope_err_rot<2 * E>(kDFTrigErrUnits);
+  constexpr float kErrAB = normrope_err_pair(kDFTrigErrUnits);
+  constexpr float kErrO = normrope_err_out<2 * E>();
+  constexpr float kErrR = normrope_err_r<2 * E>();
   __shared__ DF s_cos[HALF];
   __shared__ DF s_sin[HALF];
 
@@ -49,7 +158,20 @@ __global__ void __launch_bounds__(128) append_normrope_kernel(const __grid_const
   const int row0 = blockIdx.y * a.rows_per_cta;
   const int row1 = min(nrows, row0 + a.rows_per_cta);
   const int nr = row1 - row0;
+  if (nr <= 0) return;
 
+  // Error-bound multipliers of this lane's outputs on a roped row (bound =
+  // kA |y_self| + kB |y_other| + kO |o|): the rotation bound where the lane's
+  // pairs rotate, the plain one where none does.  A lane straddling n_rot
+  // takes the rotation bound for all its pairs, which also covers the plain ones.
+  const bool lane_plain = lane * E >= a.n_rot;
+  const float kA = lane_plain ? kErrY : kErrAB;
+  const float kB = lane_plain ? 0.0f : kErrAB;
+  const float kO = lane_plain ? 0.0f : kErrO;
+  const bool all_rot = __all_sync(0xffffffffu, (lane + 1) * E <= a.n_rot);
+
+  // This lane's cos / sin (float parts; 1 / 0 past n_rot), built per position.
+  float cr[E], sr[E];
   auto build_table = [&](int pos) {
     for (int j = threadIdx.x; j < HALF; j += blockDim.x) {
       DF c = {1.0f, 0.0f}, s = {0.0f, 0.0f};
@@ -57,9 +179,15 @@ __global__ void __launch_bounds__(128) append_normrope_kernel(const __grid_const
       s_cos[j] = c;
       s_sin[j] = s;
     }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      cr[i] = s_cos[lane * E + i].h;
+      sr[i] = s_sin[lane * E + i].h;
+    }
   };
 
-  // Where head row `row` of token (b, t) comes from and goes to.
+  // Where head row `row` of token (b, t) at position pos comes from and goes to.
   struct RowRef {
     const T* src;
     T* dst;
@@ -67,9 +195,8 @@ __global__ void __launch_bounds__(128) append_normrope_kernel(const __grid_const
     bool rope;
     bool valid;
   };
-  auto row_ref = [&](int b, int row) -> RowRef {
+  auto row_ref = [&](int b, int row, int pos) -> RowRef {
     const int tok = b * a.T + t;
-    const int pos = a.positions[tok];
     RowRef rr;
     if (row < a.H) {  // q head
       const size_t off = (static_cast<size_t>(tok) * a.H + row) * HD;
@@ -90,50 +217,168 @@ __global__ void __launch_bounds__(128) append_normrope_kernel(const __grid_const
     }
     return rr;
   };
-  auto load_row = [&](const RowRef& rr, float* x) {
+  auto load_row = [&](const RowRef& rr, HalfBits<T, E>& lo, HalfBits<T, E>& hi) {
     if (!rr.valid) return;
-    load_elems<E>(rr.src + lane * E, x);
-    load_elems<E>(rr.src + HALF + lane * E, x + E);
+    load_bits<E>(rr.src + lane * E, lo);
+    load_bits<E>(rr.src + HALF + lane * E, hi);
   };
-  auto compute_store = [&](const RowRef& rr, const float* x) {
+
+  // Values of row rr that the float32 evaluation could not decide (bit k of
+  // need: element k of the lane's 2E, lower half first), evaluated again in
+  // double-float from the row's inverse rms rd and stored over the fast ones.
+  // One element per pass, so the loop stays short for the usual 0-2 bits.
+  auto fix_elems = [&](const RowRef& rr, uint32_t need, DF rd) {
+#pragma unroll 1
+    while (need != 0) {
+      const int k = __ffs(need) - 1;
+      need &= need - 1;
+      const bool lower = k < E;
+      const int j = lane * E + (lower ? k : k - E);
+      const int self = lower ? j : HALF + j, other = lower ? HALF + j : j;
+      const float xs = static_cast<float>(rr.src[self]);
+      float v;
+      if (rr.rope) {
+        const float xo = static_cast<float>(rr.src[other]);
+        const float ws = rr.w != nullptr ? rr.w[self] : 1.0f, wo = rr.w != nullptr ? rr.w[other] : 1.0f;
+        v = normrope_exact_bf16_inl(xs, ws, xo, wo, rd, j < a.n_rot, lower, s_cos[j], s_sin[j]);
+      } else {
+        v = df_round_bf16(df_mul_f(rd, xs));
+      }
+      rr.dst[self] = static_cast<T>(v);
+    }
+  };
+
+  // Second stage for the values of row rr the float32 evaluation left open
+  // (bits of need, as for fix_elems): the same float inverse rms r times the
+  // row's inner products in double-float.  That value is off from the exact
+  // one by r's own error (and 2^-40 of the terms), much less than the float32
+  // evaluation, so it decides most of them; the bits still open are returned.
+  auto refine = [&](const RowRef& rr, uint32_t need, float r) -> uint32_t {
+    uint32_t open = 0;
+#pragma unroll 1
+    while (need != 0) {
+      const int k = __ffs(need) - 1;
+      need &= need - 1;
+      const bool lower = k < E;
+      const int j = lane * E + (lower ? k : k - E);
+      const int self = lower ? j : HALF + j, other = lower ? HALF + j : j;
+      const float xs = static_cast<float>(rr.src[self]);
+      DF inner = {xs, 0.0f};
+      float mag = fabsf(xs);
+      if (rr.rope) {
+        const float ws = rr.w != nullptr ? rr.w[self] : 1.0f;
+        inner = two_prod(xs, ws);
+        mag = fabsf(inner.h);
+        if (j < a.n_rot) {
+          const float xo = static_cast<float>(rr.src[other]);
+          const float wo = rr.w != nullptr ? rr.w[other] : 1.0f;
+          const DF po = two_prod(xo, wo);
+          mag += fabsf(po.h);
+          inner = df_add(df_mul(inner, s_cos[j]), df_mul(po, lower ? df_neg(s_sin[j]) : s_sin[j]));
+        }
+      }
+      const DF v = df_mul_f(inner, r);
+      const float e = fmaf(kErrR, fabsf(v.h), 0x1.0p-40f * r * mag);
+      if (fabsf((v.h - bf16_midpoint(v.h)) + v.l) > e)
+        rr.dst[self] = static_cast<T>(df_round_bf16(v));
+      else
+        open |= 1u << k;
+    }
+    return open;
+  };
+
+  // One row: float32 evaluation, stored.  For bf16, a value whose rounding
+  // the float32 evaluation cannot decide (Ziv's test against its error bound)
+  // is then decided in double-float (refine, then fix_elems).  all_rot (warp-uniform):
+  // every lane's pairs rotate, so both outputs of a pair share one bound.
+  auto do_row = [&](const RowRef& rr, const HalfBits<T, E>& lo, const HalfBits<T, E>& hi, auto all_rot_tag) {
+    [[maybe_unused]] constexpr bool kAllRot = decltype(all_rot_tag)::value;
     if (!rr.valid) return;
-    float wl[E], wh[E], o[2 * E];
-    if (rr.w != nullptr) {
-      load_elems<E>(rr.w + lane * E, wl);
-      load_elems<E>(rr.w + HALF + lane * E, wh);
-    } else {
+    float x[2 * E], o[2 * E];
+    unpack_bits<E>(lo, x);
+    unpack_bits<E>(hi, x + E);
+    const float sf = row_sumsq_f32<2 * E>(x);
+    const float r = inv_rms_f32(sf, HD, a.eps);
+    [[maybe_unused]] uint32_t need = 0;
+    if (rr.rope) {
+      float wl[E], wh[E], ya[E], yb[E];
+      if (rr.w != nullptr) {
+        load_elems<E>(rr.w + lane * E, wl);
+        load_elems<E>(rr.w + HALF + lane * E, wh);
+      } else {
 #pragma unroll
-      for (int i = 0; i < E; ++i) wl[i] = wh[i] = 1.0f;
-    }
-    const float r = inv_rms_f32(row_sumsq_f32<2 * E>(x), HD, a.eps);
-    uint32_t need = 0;
-#pragma unroll
-    for (int i = 0; i < E; ++i) {
-      const int j = lane * E + i;
-      const bool rot = rr.rope && j < a.n_rot;
-      bool na, nb;
-      normrope_pair_fast(x[i], wl[i], x[E + i], wh[i], r, rot, rot ? s_cos[j].h : 1.0f, rot ? s_sin[j].h : 0.0f,
-                         kErrY, kErrRot, o[i], o[E + i], na, nb);
-      need |= (na ? 1u : 0u) << i;
-      need |= (nb ? 1u : 0u) << (E + i);
-    }
-    if constexpr (kBF16) {
-      if (__any_sync(0xffffffffu, need != 0)) {
-        // Some value of this row lies too close to a bf16 rounding boundary
-        // for the float32 evaluation; decide it in double-float.
-        const DF rd = inv_rms_df(row_sumsq_df<2 * E>(x), HD, a.eps);
+        for (int i = 0; i < E; ++i) wl[i] = wh[i] = 1.0f;
+      }
+      scale_elems<E>(ya, x, r, wl);
+      scale_elems<E>(yb, x + E, r, wh);
+      rotate_elems<E>(o, o + E, ya, yb, cr, sr);
+      if constexpr (kBF16) {
 #pragma unroll
         for (int i = 0; i < E; ++i) {
-          const int j = lane * E + i;
-          const bool rot = rr.rope && j < a.n_rot;
-          if (need & (1u << i)) o[i] = normrope_exact_bf16(x[i], wl[i], x[E + i], wh[i], rd, rot, true, s_cos[j], s_sin[j]);
-          if (need & (1u << (E + i)))
-            o[E + i] = normrope_exact_bf16(x[E + i], wh[i], x[i], wl[i], rd, rot, false, s_cos[j], s_sin[j]);
+          const float aa = fabsf(ya[i]), ab = fabsf(yb[i]);
+          float ea, eb;
+          if constexpr (kAllRot) {
+            const float shared = kErrAB * (aa + ab);
+            ea = fmaf(kErrO, fabsf(o[i]), shared);
+            eb = fmaf(kErrO, fabsf(o[E + i]), shared);
+          } else {
+            ea = fmaf(kO, fabsf(o[i]), fmaf(kB, ab, kA * aa));
+            eb = fmaf(kO, fabsf(o[E + i]), fmaf(kB, aa, kA * ab));
+          }
+          need |= (bf16_decided(o[i], ea) ? 0u : 1u) << i;
+          need |= (bf16_decided(o[E + i], eb) ? 0u : 1u) << (E + i);
         }
+      }
+    } else {  // v head: weight-less norm, no rotation
+      scale_elems<E>(o, x, r, nullptr);
+      scale_elems<E>(o + E, x + E, r, nullptr);
+      if constexpr (kBF16) {
+#pragma unroll
+        for (int k = 0; k < 2 * E; ++k) need |= (bf16_decided(o[k], kErrY * fabsf(o[k])) ? 0u : 1u) << k;
       }
     }
     store_elems<E>(rr.dst + lane * E, o);
     store_elems<E>(rr.dst + HALF + lane * E, o + E);
+    if constexpr (kBF16) {
+      if (__any_sync(0xffffffffu, need != 0)) {
+        need = refine(rr, need, r);
+        if (__any_sync(0xffffffffu, need != 0))
+          fix_elems(rr, need, inv_rms_df(row_sumsq_split<2 * E, HD>(x, sf), HD, a.eps));
+      }
+    }
+  };
+
+  // Rows of tokens [bA, bB) (all at position pos), flattened in (b, row)
+  // order; warp w takes items w, w + 4, ...  The next item's loads are issued
+  // before the current one is computed.
+  auto run = [&](int bA, int bB, int pos) {
+    int b = bA, row = row0 + warp;
+    while (row >= row1 && b < bB) { row -= nr; ++b; }
+    RowRef rr = {};
+    HalfBits<T, E> lo, hi;
+    if (b < bB) {
+      rr = row_ref(b, row, pos);
+      load_row(rr, lo, hi);
+    }
+    while (b < bB) {
+      int bn = b, rn = row + 4;
+      while (rn >= row1 && bn < bB) { rn -= nr; ++bn; }
+      RowRef rrn = {};
+      HalfBits<T, E> lon, hin;
+      if (bn < bB) {
+        rrn = row_ref(bn, rn, pos);
+        load_row(rrn, lon, hin);
+      }
+      if (all_rot)
+        do_row(rr, lo, hi, std::true_type());
+      else
+        do_row(rr, lo, hi, std::false_type());
+      b = bn;
+      row = rn;
+      rr = rrn;
+      lo = lon;
+      hi = hin;
+    }
   };
 
   // One cos/sin table serves every token of the CTA when their positions
@@ -143,24 +388,13 @@ __global__ void __launch_bounds__(128) append_normrope_kernel(const __grid_const
   for (int b = b0 + 1; b < b1; ++b) same = same && a.positions[b * a.T + t] == p0;
   if (same) {
     build_table(p0);
-    __syncthreads();
-    for (int idx = warp; idx < (b1 - b0) * nr; idx += 4) {
-      const RowRef rr = row_ref(b0 + idx / nr, row0 + idx % nr);
-      float x[2 * E];
-      load_row(rr, x);
-      compute_store(rr, x);
-    }
+    run(b0, b1, p0);
   } else {
     for (int b = b0; b < b1; ++b) {
-      if (b > b0) __syncthreads();
-      build_table(a.positions[b * a.T + t]);
-      __syncthreads();
-      for (int row = row0 + warp; row < row1; row += 4) {
-        const RowRef rr = row_ref(b, row);
-        float x[2 * E];
-        load_row(rr, x);
-        compute_store(rr, x);
-      }
+      if (b > b0) __syncthreads();  // every warp is done with the previous table
+      const int pos = a.positions[b * a.T + t];
+      build_table(pos);
+      run(b, b + 1, pos);
     }
   }
 }

@@ -18,7 +18,8 @@
 //   * otherwise a double-float evaluation decides: values carried as an
 //     unevaluated sum of two floats, built from Dekker's exact product (one
 //     fma) and Knuth's two-sum, accurate to about 2^-44 relative.  It runs
-//     for well under one element in a thousand.
+//     for about one element in a thousand (rotated values whose two terms
+//     nearly cancel make up most of them).
 // cos / sin in double-float come from an exact p * f, Cody-Waite reduction
 // by a three-float pi/2 and Taylor polynomials on [-pi/4, pi/4].
 #pragma once
@@ -139,6 +140,61 @@ __device__ __forceinline__ DF row_sumsq_df(const float* x) {
   return s;
 }
 
+// The same row sum in double-float, cheaper, for rows whose squares are exact
+// in float (bf16 elements) and whose float32 sum sf (row_sumsq_f32) is known.
+// Two error-free splittings against powers of two (Rump, Ogita and Oishi's
+// ExtractScalar): each square p = q1 + q2 + p2 exactly, q1 a multiple of
+// ulp(s1), q2 of ulp(s2) / 2, with s1 >= 2 sf and s2 = s1 2^(log2 HD - 23).
+// Every partial sum of the q1 (and of the q2) is then exact in float, and the
+// p2 are small enough (|p2| <= s2 2^-24) that their float sum is off by less
+// than 2^-46 of the row sum.  Rows outside [2^-60, 2^124) take row_sumsq_df.
+template <int N, int HD>
+__device__ __forceinline__ DF row_sumsq_split(const float* x, float sf) {
+  if (!(sf >= 0x1.0p-60f && sf < 0x1.0p+124f)) return row_sumsq_df<N>(x);
+  const float s1 = __uint_as_float((__float_as_uint(sf) & 0x7F800000u) + (2u << 23));  // 2^(e+2) > 2 sf
+  const float s2 = s1 * (static_cast<float>(HD) * 0x1.0p-23f);
+  float a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+  if constexpr (N % 2 == 0) {
+    float2 c1 = make_float2(0.0f, 0.0f), c2 = c1, c3 = c1;
+    const float2 ps1 = make_float2(s1, s1), ns1 = make_float2(-s1, -s1);
+    const float2 ps2 = make_float2(s2, s2), ns2 = make_float2(-s2, -s2);
+    const float2 m1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+    for (int i = 0; i < N; i += 2) {
+      const float2 v = make_float2(x[i], x[i + 1]);
+      const float2 p = __fmul2_rn(v, v);
+      const float2 q1 = __fadd2_rn(__fadd2_rn(ps1, p), ns1);
+      const float2 r1 = __ffma2_rn(q1, m1, p);
+      const float2 q2 = __fadd2_rn(__fadd2_rn(ps2, r1), ns2);
+      const float2 r2 = __ffma2_rn(q2, m1, r1);
+      c1 = __fadd2_rn(c1, q1);
+      c2 = __fadd2_rn(c2, q2);
+      c3 = __fadd2_rn(c3, r2);
+    }
+    a1 = c1.x + c1.y;
+    a2 = c2.x + c2.y;
+    a3 = c3.x + c3.y;
+  } else {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      const float p = x[i] * x[i];
+      const float q1 = (s1 + p) - s1;
+      const float r1 = p - q1;
+      const float q2 = (s2 + r1) - s2;
+      a1 += q1;
+      a2 += q2;
+      a3 += r1 - q2;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+    a2 += __shfl_xor_sync(0xffffffffu, a2, o);
+    a3 += __shfl_xor_sync(0xffffffffu, a3, o);
+  }
+  return df_add_f(fast_two_sum(a1, a2), a3);
+}
+
 // (sumsq / hd + eps)^(-1/2) in double-float: one Newton step on rsqrtf.
 __device__ __forceinline__ DF inv_rms_df(DF sumsq, int hd, float eps) {
   const float inv_hd = 1.0f / static_cast<float>(hd);  // hd is a power of two: exact
@@ -216,12 +272,16 @@ constexpr float kDFTrigErrUnits = 1.0f;
 
 // Exact value of one output of a pair, rounded to bf16: y_self * c +- y_other
 // * s on a rotated pair (sign - for the lower element), else y_self.
-static __device__ __noinline__ float normrope_exact_bf16(float x_self, float w_self, float x_other, float w_other, DF r,
+__device__ __forceinline__ float normrope_exact_bf16_inl(float x_self, float w_self, float x_other, float w_other, DF r,
                                                          bool rot, bool lower, DF c, DF s) {
   const DF ys = df_mul_f(df_mul_f(r, x_self), w_self);
   if (!rot) return df_round_bf16(ys);
   const DF yo = df_mul_f(df_mul_f(r, x_other), w_other);
   return df_round_bf16(df_add(df_mul(ys, c), df_mul(yo, lower ? df_neg(s) : s)));
+}
+static __device__ __noinline__ float normrope_exact_bf16(float x_self, float w_self, float x_other, float w_other, DF r,
+                                                         bool rot, bool lower, DF c, DF s) {
+  return normrope_exact_bf16_inl(x_self, w_self, x_other, w_other, r, rot, lower, c, s);
 }
 
 // Float32 evaluation of one pair (lower a = element j, upper b = element
@@ -249,15 +309,43 @@ __device__ __forceinline__ void normrope_pair_fast(float xa, float wa, float xb,
   need_b = !(fabsf(ob - bf16_midpoint(ob)) > eb);
 }
 
-// Bounds for normrope_pair_fast with N elements per lane, the cos / sin error
-// trig_units, and a 1.5x margin.
+// Bounds for normrope_pair_fast with N elements per lane and the cos / sin
+// error trig_units.  To first order the error of a plain output is
+// norm_err_units u |y|; that of a rotated one, ya c - yb s with c, s off by
+// trig_units u relative, the product yb s and the fma each rounded once, is
+// at most (norm_err_units + trig_units + 2) u (|ya c| + |yb s|), so (as
+// |c|, |s| <= 1) at most that times |ya| + |yb|.  The factor 1 + 2^-4 covers the second-order terms (below 2^-40
+// relative), the rounding of the bound itself and |y| standing for the exact
+// normed value (both below 2^-19 relative).
+constexpr float kBoundMargin = 1.0625f;
 template <int N>
 constexpr float normrope_err_y() {
-  return 1.5f * norm_err_units<N>() * 0x1.0p-24f;
+  return kBoundMargin * norm_err_units<N>() * 0x1.0p-24f;
 }
 template <int N>
 constexpr float normrope_err_rot(float trig_units) {
-  return 1.5f * (norm_err_units<N>() + trig_units + 2.0f) * 0x1.0p-24f;
+  return kBoundMargin * (norm_err_units<N>() + trig_units + 2.0f) * 0x1.0p-24f;
+}
+
+// A sharper bound for a rotated output, split by where the error comes from.
+// With r_f the float32 inverse rms as computed, let O' = r_f (xa wa c - xb wb
+// s) in exact arithmetic.  The float32 evaluation is within (3 + trig_units) u
+// (|ya| + |yb|) of O' (two roundings in each y, the table's cos / sin, the
+// product yb s) plus u |o| (the fma); O' is within (norm_err_units - 2) u |o|
+// of the exact value, r_f's own relative error being the sum's, the eps
+// addition's and the root's.  So the bound is
+//   normrope_err_pair * (|ya| + |yb|) + normrope_err_out * |o|,
+// never above normrope_err_rot * (|ya| + |yb|) and about half of it on average.
+constexpr float normrope_err_pair(float trig_units) { return kBoundMargin * (3.0f + trig_units) * 0x1.0p-24f; }
+template <int N>
+constexpr float normrope_err_out() {
+  return kBoundMargin * (norm_err_units<N>() - 1.0f) * 0x1.0p-24f;
+}
+// Bound (times |o|) on the error of r_f times an inner product evaluated in
+// double-float: r_f's relative error alone.
+template <int N>
+constexpr float normrope_err_r() {
+  return kBoundMargin * (norm_err_units<N>() - 2.0f) * 0x1.0p-24f;
 }
 
 // Inverse rms of a row in float32 (all lanes), from row_sumsq_f32.
