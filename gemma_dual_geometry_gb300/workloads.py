@@ -17,6 +17,9 @@ The five workloads are the ones the attention path is specified on:
 * ``longctx_decode_bf16`` -- batch 4, KV length 131072 on the full layer plus a
   sliding layer.
 
+``stack42_bf16_dec8`` is ``stack42_bf16`` with 8 decode steps, for launch lists
+taken under a profiler.
+
 Values: q/k/v and cache contents ~ N(0, 1); norm weights ~ 1 + 0.1 N(0, 1)
 (float32).  bf16 workloads round the float32 draws to bf16 (torch's RNE cast).
 """
@@ -47,6 +50,13 @@ CONFIGS = {
         geom={SLIDING: SLIDING_GEOM_BF16, FULL: FULL_GEOM_BF16}),
     "stack42_bf16": dict(
         B=8, T=4096, decode_steps=128, H=8, Hkv=2, dtype=BF16, seed=3,
+        types=[FULL if (i + 1) % 6 == 0 else SLIDING for i in range(42)], n_shared=18,
+        geom={SLIDING: SLIDING_GEOM_BF16, FULL: FULL_GEOM_BF16}),
+    # The same 42-layer stack with an 8-step decode phase, for launch lists
+    # under a profiler: every decode step launches the same kernels, so the
+    # 128-step figures are the decode launches' times x 16.
+    "stack42_bf16_dec8": dict(
+        B=8, T=4096, decode_steps=8, H=8, Hkv=2, dtype=BF16, seed=3,
         types=[FULL if (i + 1) % 6 == 0 else SLIDING for i in range(42)], n_shared=18,
         geom={SLIDING: SLIDING_GEOM_BF16, FULL: FULL_GEOM_BF16}),
     "longctx_decode_bf16": dict(
