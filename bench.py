@@ -277,7 +277,7 @@ class Job:
         torch = self.torch
         events = {}
         try:
-            for s in DECODE_EVENT_STEPS:
+            for s in sorted({s for s in DECODE_EVENT_STEPS if s < self.S} | {self.S - 1}):
                 for l in self.full_layers:
                     events[(s, l)] = (torch.cuda.Event(enable_timing=True, external=True),
                                       torch.cuda.Event(enable_timing=True, external=True))
