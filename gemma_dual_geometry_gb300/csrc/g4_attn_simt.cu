@@ -10,8 +10,9 @@
 //
 // Work decomposition: one CTA per (split, kv head, query row).  All G query
 // heads of the kv head share every K/V row the CTA streams, so each key row
-// is read from HBM once per query row.  Each of the 4 warps owns a ring of
-// 3 shared-memory stages filled by non-tensor bulk copies
+// is read from HBM once per query row.  Each of the 4 warps (8 when the
+// launch fits one CTA per SM) owns a ring of 2-3 shared-memory stages filled
+// by non-tensor bulk copies
 // (cp.async.bulk, one K and one V copy per stage, completing on the stage's
 // mbarrier); stages of the CTA's key range go to the warps round-robin.
 //
@@ -45,7 +46,6 @@
 namespace g4 {
 namespace {
 
-constexpr int kNW = 4;            // warps per CTA
 constexpr int kNPMax = 16;        // partial scores per reduce-scatter batch, at most
 constexpr int kStageMaxB = 4096;  // bytes of K (and of V) a reduce batch may span
 
@@ -92,8 +92,9 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[NP], int lane) {
   return r;
 }
 
-template <typename T, int HD, int G>
+template <typename T, int HD, int G, int NW_>
 struct SimtCfg {
+  static constexpr int NW = NW_;                     // warps per CTA
   static constexpr int ES = sizeof(T);
   static constexpr int EL = HD / 32;                 // elements per lane per row
   static constexpr int CHE = 16 / ES;                // elements per 16-byte piece
@@ -108,21 +109,23 @@ struct SimtCfg {
   static constexpr int SK = KB * NB;                 // keys per stage
   static constexpr int STAGE_B = SK * ROWB;          // bytes of K (and of V) per stage
   // G*HD = 2048 needs ~180 registers for q and o alone: two CTAs per SM with
-  // three stages per warp; narrower heads fit three CTAs with two stages.
+  // three stages per warp; narrower heads fit three CTAs with two stages.  The
+  // 8-warp CTA serves launches of at most one CTA per SM.
   static constexpr int NST = (G * HD >= 2048) ? 3 : 2;   // stages per warp
-  static constexpr int MINB = (G * HD >= 2048) ? 2 : 3;  // CTAs per SM the register budget aims for
-  static constexpr int RING_B = kNW * NST * 2 * STAGE_B;
-  static constexpr int MERGE_B = kNW * G * (HD + 2) * 4;
+  static constexpr int MINB = NW > 4 ? 1 : (G * HD >= 2048) ? 2 : 3;  // CTAs per SM the register budget aims for
+  static constexpr int RING_B = NW * NST * 2 * STAGE_B;
+  static constexpr int MERGE_B = NW * G * (HD + 2) * 4;
   static constexpr int AREA_B = RING_B > MERGE_B ? RING_B : MERGE_B;
   // after the area: barriers, per-warp score buffers, cos/sin table, merge weights, flag
   static constexpr int BAR_OFF = AREA_B;
-  static constexpr int SC_OFF = BAR_OFF + kNW * NST * 8;
-  static constexpr int SA_OFF = SC_OFF + kNW * kNPMax * 4;
-  static constexpr int COS_OFF = SA_OFF + kNW * 8 * 4;
+  static constexpr int SC_OFF = BAR_OFF + NW * NST * 8;
+  static constexpr int SA_OFF = SC_OFF + NW * kNPMax * 4;
+  static constexpr int COS_OFF = SA_OFF + NW * 8 * 4;
   static constexpr int W_OFF = COS_OFF + HD * 8;  // cos and sin of HD/2 pairs, double-float
   static constexpr int FLAG_OFF = W_OFF + G * kMaxSplits * 4;
   static constexpr int QN_OFF = FLAG_OFF + 16;  // normed q of the G heads (fused step)
-  static constexpr int SMEM_B = QN_OFF + G * HD * ES;
+  static constexpr int KN_OFF = QN_OFF + G * HD * ES;  // normed new k and v (fused step)
+  static constexpr int SMEM_B = KN_OFF + 2 * HD * ES;
   static_assert(NP >= 2 && NP <= 16 && (NP & (NP - 1)) == 0, "reduce batch");
   static_assert(SMEM_B <= 232448, "shared memory budget");
 };
@@ -164,18 +167,25 @@ __device__ __forceinline__ float through(float x) {
 }
 
 // RMSNorm (optional weight) then rotate_half RoPE of one row held in the lane
-// layout above, at position pos; the partner of element d is d +- HD/2, which
-// is the same lane (NPC >= 2) or lane ^ 16 (NPC == 1).  bf16 results are the
-// correctly rounded real values (g4_normrope.cuh), the ones the append
-// kernel stores.  s_cos / s_sin hold cos and sin of the HD/2 pairs.
+// layout above (src: the same row in memory), at position pos; the partner
+// of element d is d +- HD/2, which is the same lane (NPC >= 2) or lane ^ 16
+// (NPC == 1).  bf16 results are the correctly rounded real values
+// (g4_normrope.cuh), the ones the append kernel stores, decided in three
+// stages as there: float32 with Ziv's test; the float inverse rms times the
+// inner products in double-float for the values left open; the row's
+// double-float inverse rms for the rest.  s_cos / s_sin hold cos and sin of
+// the HD/2 pairs.
 template <typename T, int HD, int NPC, int PE>
-__device__ __forceinline__ void norm_rope_row(float* f, const float* w, bool rope, const DF* s_cos, const DF* s_sin,
-                                              int n_rot, float eps, int lane) {
+__device__ __forceinline__ void norm_rope_row(float* f, const T* src, const float* w, bool rope, const DF* s_cos,
+                                              const DF* s_sin, int n_rot, float eps, int lane) {
   constexpr int EL = NPC * PE;
   constexpr bool kBF16 = sizeof(T) == 2;
   constexpr float kErrY = normrope_err_y<EL>();
-  constexpr float kErrRot = normrope_err_rot<EL>(kDFTrigErrUnits);
-  const float r = inv_rms_f32(row_sumsq_f32<EL>(f), HD, eps);
+  constexpr float kErrAB = normrope_err_pair(kDFTrigErrUnits);
+  constexpr float kErrO = normrope_err_out<EL>();
+  constexpr float kErrR = normrope_err_r<EL>();
+  const float sf = row_sumsq_f32<EL>(f);
+  const float r = inv_rms_f32(sf, HD, eps);
   float wf[EL];
   if (w != nullptr) {
     load_row<float, NPC, PE>(w, lane, wf);
@@ -215,11 +225,11 @@ __device__ __forceinline__ void norm_rope_row(float* f, const float* w, bool rop
       float oa, ob;
       bool na, nb;
       if (lower) {
-        normrope_pair_fast(f[i], wf[i], fp[i], wp[i], r, rot, t.x, t.y, kErrY, kErrRot, oa, ob, na, nb);
+        normrope_pair_fast(f[i], wf[i], fp[i], wp[i], r, rot, t.x, t.y, kErrY, kErrAB, kErrO, oa, ob, na, nb);
         o[i] = oa;
         need |= (na ? 1u : 0u) << i;
       } else {
-        normrope_pair_fast(fp[i], wp[i], f[i], wf[i], r, rot, t.x, t.y, kErrY, kErrRot, oa, ob, na, nb);
+        normrope_pair_fast(fp[i], wp[i], f[i], wf[i], r, rot, t.x, t.y, kErrY, kErrAB, kErrO, oa, ob, na, nb);
         o[i] = ob;
         need |= (nb ? 1u : 0u) << i;
       }
@@ -227,17 +237,47 @@ __device__ __forceinline__ void norm_rope_row(float* f, const float* w, bool rop
   }
   if constexpr (kBF16) {
     if (__any_sync(0xffffffffu, need != 0)) {
-      const DF rd = inv_rms_df(row_sumsq_df<EL>(f), HD, eps);
+      // Stage 2, lane by lane, one open value per pass (operands reloaded).
+      uint32_t open = 0;
+#pragma unroll 1
+      for (uint32_t left = need; left != 0; left &= left - 1) {
+        const int i = __ffs(left) - 1;
+        const int d = (lane + 32 * (i / PE)) * PE + i % PE;
+        const bool lower = d < HD / 2;
+        const int j = lower ? d : d - HD / 2;
+        const int other = lower ? d + HD / 2 : d - HD / 2;
+        const float xs = static_cast<float>(src[d]);
+        DF inner = two_prod(xs, w != nullptr ? w[d] : 1.0f);
+        float mag = fabsf(inner.h);
+        if (rope && j < n_rot) {
+          const DF po = two_prod(static_cast<float>(src[other]), w != nullptr ? w[other] : 1.0f);
+          mag += fabsf(po.h);
+          inner = df_add(df_mul(inner, s_cos[j]), df_mul(po, lower ? df_neg(s_sin[j]) : s_sin[j]));
+        }
+        const DF v = df_mul_f(inner, r);
+        if (fabsf((v.h - bf16_midpoint(v.h)) + v.l) > fmaf(kErrR, fabsf(v.h), 0x1.0p-40f * r * mag)) {
+          const float val = df_round_bf16(v);
 #pragma unroll
-      for (int c = 0; c < NPC; ++c) {
+          for (int k = 0; k < EL; ++k)
+            if (k == i) o[k] = val;
+        } else {
+          open |= 1u << i;
+        }
+      }
+      // Stage 3: the row's double-float inverse rms.
+      if (__any_sync(0xffffffffu, open != 0)) {
+        const DF rd = inv_rms_df(row_sumsq_split<EL, HD>(f, sf), HD, eps);
 #pragma unroll
-        for (int e = 0; e < PE; ++e) {
-          const int i = c * PE + e;
-          if (need & (1u << i)) {
-            const int d = (lane + 32 * c) * PE + e;
-            const bool lower = d < HD / 2;
-            const int j = lower ? d : d - HD / 2;
-            o[i] = normrope_exact_bf16(f[i], wf[i], fp[i], wp[i], rd, rope && j < n_rot, lower, s_cos[j], s_sin[j]);
+        for (int c = 0; c < NPC; ++c) {
+#pragma unroll
+          for (int e = 0; e < PE; ++e) {
+            const int i = c * PE + e;
+            if (open & (1u << i)) {
+              const int d = (lane + 32 * c) * PE + e;
+              const bool lower = d < HD / 2;
+              const int j = lower ? d : d - HD / 2;
+              o[i] = normrope_exact_bf16(f[i], wf[i], fp[i], wp[i], rd, rope && j < n_rot, lower, s_cos[j], s_sin[j]);
+            }
           }
         }
       }
@@ -248,10 +288,10 @@ __device__ __forceinline__ void norm_rope_row(float* f, const float* w, bool rop
   for (int i = 0; i < EL; ++i) f[i] = through<T>(o[i]);
 }
 
-template <typename T, int HD, int G, bool FUSED>
-__global__ void __launch_bounds__(kNW * 32, (SimtCfg<T, HD, G>::MINB))
+template <typename T, int HD, int G, bool FUSED, int NW>
+__global__ void __launch_bounds__(NW * 32, (SimtCfg<T, HD, G, NW>::MINB))
     attn_simt_kernel(const __grid_constant__ AttnSimtArgs a) {
-  using C = SimtCfg<T, HD, G>;
+  using C = SimtCfg<T, HD, G, NW>;
   constexpr int EL2 = C::EL / 2;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -320,29 +360,54 @@ __global__ void __launch_bounds__(kNW * 32, (SimtCfg<T, HD, G>::MINB))
 
   if (lane == 0) {
     for (int i = 0; i < C::NST; ++i) {
-      const int st = warp + i * kNW;
+      const int st = warp + i * NW;
       if (st < nstages) issue(st, i);
     }
   }
 
   if constexpr (FUSED) {
-    // cos/sin of the new token's position, then its q heads normed and
-    // roped once per CTA (warp w takes heads w, w + 4, ...) into shared memory
+    // cos/sin of the new token's position (two threads per rotated pair, one
+    // per polynomial), then its q heads -- and on the CTA that holds position
+    // L-1 the new k and v -- normed and roped, one row per warp, into shared
+    // memory (k and v also into the cache row L-1).
     const int pos = L - 1;
-    for (int j = threadIdx.x; j < HD / 2; j += blockDim.x) {
-      DF c = {1.0f, 0.0f}, s = {0.0f, 0.0f};
-      if (j < a.n_rot) sincos_df(pos, a.inv_freq[j], c, s);
-      s_cos[j] = c;
-      s_sin[j] = s;
+    for (int idx = threadIdx.x; idx < HD; idx += blockDim.x) {
+      const int j = idx >> 1, part = idx & 1;
+      if (j < a.n_rot) {
+        bool to_cos;
+        const DF v = sincos_df_part(pos, a.inv_freq[j], part, to_cos);
+        (to_cos ? s_cos : s_sin)[j] = v;
+      } else if (part == 0) {
+        s_cos[j] = DF{1.0f, 0.0f};
+      } else {
+        s_sin[j] = DF{0.0f, 0.0f};
+      }
     }
     __syncthreads();
     T* s_qn = reinterpret_cast<T*>(smem + C::QN_OFF);
-    for (int h = warp; h < G; h += kNW) {
-      const T* qrow = static_cast<const T*>(a.q) + (static_cast<size_t>(bt) * a.H + kvh * G + h) * HD;
+    T* s_kn = reinterpret_cast<T*>(smem + C::KN_OFF);
+    const int njobs = G + (new_key ? 2 : 0);
+    for (int job = warp; job < njobs; job += NW) {
+      const T* src;
+      T* dst_g = nullptr;
+      const float* wgt = a.q_w;
+      bool rope = true;
+      if (job < G) {
+        src = static_cast<const T*>(a.q) + (static_cast<size_t>(bt) * a.H + kvh * G + job) * HD;
+      } else {
+        const size_t raw = (static_cast<size_t>(b) * a.Hkv + kvh) * HD;
+        const size_t row = (head_base + (L - 1)) * HD;
+        const bool is_k = job == G;
+        src = static_cast<const T*>(is_k ? a.k_raw : a.v_raw) + raw;
+        dst_g = static_cast<T*>(is_k ? a.cache_k : a.cache_v) + row;
+        wgt = is_k ? a.k_w : nullptr;
+        rope = is_k;
+      }
       float f[C::EL];
-      load_row<T, C::NPC, C::PE>(qrow, lane, f);
-      norm_rope_row<T, HD, C::NPC, C::PE>(f, a.q_w, true, s_cos, s_sin, a.n_rot, a.eps, lane);
-      store_row<T, C::NPC, C::PE>(s_qn + h * HD, lane, f);
+      load_row<T, C::NPC, C::PE>(src, lane, f);
+      norm_rope_row<T, HD, C::NPC, C::PE>(f, src, wgt, rope, s_cos, s_sin, a.n_rot, a.eps, lane);
+      store_row<T, C::NPC, C::PE>(job < G ? s_qn + job * HD : s_kn + (job - G) * HD, lane, f);
+      if (dst_g != nullptr) store_row<T, C::NPC, C::PE>(dst_g, lane, f);
     }
     __syncthreads();
   }
@@ -368,9 +433,41 @@ __global__ void __launch_bounds__(kNW * 32, (SimtCfg<T, HD, G>::MINB))
     for (int i = 0; i < EL2; ++i) o2[h][i] = make_float2(0.0f, 0.0f);
   }
 
+  if constexpr (FUSED) {
+    // The new key (normed above) goes first, into the last warp's state.
+    if (new_key && warp == NW - 1) {
+      const T* s_kn = reinterpret_cast<const T*>(smem + C::KN_OFF);
+      float2 kx[EL2], vx[EL2];
+      load_row_f2<T, C::NPC, C::PE>(s_kn, lane, kx);
+      load_row_f2<T, C::NPC, C::PE>(s_kn + HD, lane, vx);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int i = 0; i < EL2; ++i) acc = fma2(q2[h][i], kx[i], acc);
+        const float s = warp_sum(acc.x + acc.y);
+        const float m_h = __shfl_sync(0xffffffffu, m_l, h << kSh);
+        const float m_new = fmaxf(m_h, s);
+        const float alpha = (m_h == -INFINITY) ? 0.0f : ex2(m_h - m_new);
+        const float pn = ex2(s - m_new);
+        if (hh == h) {
+          l_l = l_l * alpha + pn;
+          m_l = m_new;
+        }
+        const float2 pp = make_float2(pn, pn);
+#pragma unroll
+        for (int i = 0; i < EL2; ++i) {
+          o2[h][i].x *= alpha;
+          o2[h][i].y *= alpha;
+          o2[h][i] = fma2(pp, vx[i], o2[h][i]);
+        }
+      }
+    }
+  }
+
   int consumed = 0;  // stages this warp has finished (for draining after an abort)
   for (int it = 0;; ++it) {
-    const int st_idx = warp + it * kNW;
+    const int st_idx = warp + it * NW;
     if (st_idx >= nstages) break;
     const int buf = it % C::NST;
     if (!warp_wait(smem_u32(&wbar[buf]), (it / C::NST) & 1, a.err)) {
@@ -454,64 +551,25 @@ __global__ void __launch_bounds__(kNW * 32, (SimtCfg<T, HD, G>::MINB))
     }
     __syncwarp();
     consumed = it + 1;
-    const int next = st_idx + C::NST * kNW;
+    const int next = st_idx + C::NST * NW;
     if (lane == 0 && next < nstages) issue(next, buf);
   }
 
   // After an abort, wait (bounded) for copies this warp still has in flight.
   if (aborted) {
     for (int it = consumed;; ++it) {
-      const int st_idx = warp + it * kNW;
+      const int st_idx = warp + it * NW;
       if (st_idx >= nstages || it >= consumed + C::NST) break;
       warp_wait(smem_u32(&wbar[it % C::NST]), (it / C::NST) & 1, nullptr);
     }
   }
 
-  if constexpr (FUSED) {
-    if (new_key && warp == 0) {
-      // the new token's k and v: normed (+ roped for k), stored at row L-1, used as a key
-      const size_t row = (head_base + (L - 1)) * HD;
-      const size_t raw = (static_cast<size_t>(b) * a.Hkv + kvh) * HD;
-      float kf[C::EL], vf[C::EL];
-      load_row<T, C::NPC, C::PE>(static_cast<const T*>(a.k_raw) + raw, lane, kf);
-      load_row<T, C::NPC, C::PE>(static_cast<const T*>(a.v_raw) + raw, lane, vf);
-      norm_rope_row<T, HD, C::NPC, C::PE>(kf, a.k_w, true, s_cos, s_sin, a.n_rot, a.eps, lane);
-      norm_rope_row<T, HD, C::NPC, C::PE>(vf, nullptr, false, s_cos, s_sin, a.n_rot, a.eps, lane);
-      store_row<T, C::NPC, C::PE>(static_cast<T*>(a.cache_k) + row, lane, kf);
-      store_row<T, C::NPC, C::PE>(static_cast<T*>(a.cache_v) + row, lane, vf);
-      float2 kx[EL2], vx[EL2];
-      to_f2<C::EL>(kf, kx);
-      to_f2<C::EL>(vf, vx);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int i = 0; i < EL2; ++i) acc = fma2(q2[h][i], kx[i], acc);
-        const float s = warp_sum(acc.x + acc.y);
-        const float m_h = __shfl_sync(0xffffffffu, m_l, h << kSh);
-        const float m_new = fmaxf(m_h, s);
-        const float alpha = (m_h == -INFINITY) ? 0.0f : ex2(m_h - m_new);
-        const float pn = ex2(s - m_new);
-        if (hh == h) {
-          l_l = l_l * alpha + pn;
-          m_l = m_new;
-        }
-        const float2 pp = make_float2(pn, pn);
-#pragma unroll
-        for (int i = 0; i < EL2; ++i) {
-          o2[h][i].x *= alpha;
-          o2[h][i].y *= alpha;
-          o2[h][i] = fma2(pp, vx[i], o2[h][i]);
-        }
-      }
-    }
-  }
   __syncthreads();
 
   // Merge the warps' (m, l, o) through shared memory (the ring is free now).
   float* ms = reinterpret_cast<float*>(smem);          // [NW][G]
-  float* ls = ms + kNW * G;                            // [NW][G]
-  float* os = ls + kNW * G;                            // [NW][G][HD]
+  float* ls = ms + NW * G;                            // [NW][G]
+  float* os = ls + NW * G;                            // [NW][G][HD]
   if ((lane & ((1 << kSh) - 1)) == 0 && (lane >> kSh) < G) {
     ms[warp * G + hh] = m_l;
     ls[warp * G + hh] = l_l;
@@ -537,11 +595,11 @@ __global__ void __launch_bounds__(kNW * 32, (SimtCfg<T, HD, G>::MINB))
     const int d = idx % HD;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kNW; ++w) M = fmaxf(M, ms[w * G + h]);
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, ms[w * G + h]);
     float O = 0.0f, Ls = 0.0f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kNW; ++w) {
+      for (int w = 0; w < NW; ++w) {
         const float mw = ms[w * G + h];
         if (mw != -INFINITY) {
           const float f = ex2(mw - M);
@@ -575,7 +633,7 @@ __global__ void __launch_bounds__(kNW * 32, (SimtCfg<T, HD, G>::MINB))
   __syncthreads();
   if (*s_flag == 0) return;
   __threadfence();
-  for (int h = warp; h < G; h += kNW) {
+  for (int h = warp; h < G; h += NW) {
     const size_t p0 = (static_cast<size_t>(bt) * a.H + kvh * G + h) * a.nsplit;
     float M = -INFINITY;
     for (int s = lane; s < a.nsplit; s += 32) M = fmaxf(M, __ldcg(a.ws_m + p0 + s));
@@ -597,7 +655,7 @@ __global__ void __launch_bounds__(kNW * 32, (SimtCfg<T, HD, G>::MINB))
   // Each thread owns float4 groups of the G*HD outputs and keeps many loads in
   // flight: 8 splits x up to 4 groups per round.
   constexpr int NG4 = G * HD / 4;                        // float4 groups
-  constexpr int PER = (NG4 + kNW * 32 - 1) / (kNW * 32);  // groups per thread
+  constexpr int PER = (NG4 + NW * 32 - 1) / (NW * 32);  // groups per thread
   float4 acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -606,7 +664,7 @@ __global__ void __launch_bounds__(kNW * 32, (SimtCfg<T, HD, G>::MINB))
     float4 v[PER][8];
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
-      const int g4i = threadIdx.x + i * kNW * 32;
+      const int g4i = threadIdx.x + i * NW * 32;
       const int h = (g4i * 4) / HD;
       const int d = (g4i * 4) % HD;
 #pragma unroll
@@ -620,7 +678,7 @@ __global__ void __launch_bounds__(kNW * 32, (SimtCfg<T, HD, G>::MINB))
     }
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
-      const int g4i = threadIdx.x + i * kNW * 32;
+      const int g4i = threadIdx.x + i * NW * 32;
       const int h = g4i < NG4 ? (g4i * 4) / HD : 0;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -634,7 +692,7 @@ __global__ void __launch_bounds__(kNW * 32, (SimtCfg<T, HD, G>::MINB))
   }
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
-    const int g4i = threadIdx.x + i * kNW * 32;
+    const int g4i = threadIdx.x + i * NW * 32;
     if (g4i < NG4) {
       const int h = (g4i * 4) / HD;
       const int d = (g4i * 4) % HD;
@@ -662,18 +720,27 @@ cudaError_t launch_pdl(Kern kern, unsigned grid, unsigned block, size_t smem, cu
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <typename T, int HD, int G, bool FUSED>
-cudaError_t launch_simt_hgf(const AttnSimtArgs& a, cudaStream_t s) {
-  using C = SimtCfg<T, HD, G>;
+template <typename T, int HD, int G, bool FUSED, int NW>
+cudaError_t launch_simt_hgfw(const AttnSimtArgs& a, long long nblk, cudaStream_t s) {
+  using C = SimtCfg<T, HD, G, NW>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, HD, G, FUSED>,
+    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, HD, G, FUSED, NW>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_B);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  return launch_pdl(attn_simt_kernel<T, HD, G, FUSED, NW>, static_cast<unsigned>(nblk), NW * 32, C::SMEM_B, s, a);
+}
+
+// A launch that fits one CTA per SM (short sliding windows, small batches)
+// is latency-bound: its CTAs take 8 warps, so each warp streams half as many
+// stages.  Larger launches keep 4 warps and several CTAs per SM.
+template <typename T, int HD, int G, bool FUSED>
+cudaError_t launch_simt_hgf(const AttnSimtArgs& a, cudaStream_t s) {
   const long long nblk = static_cast<long long>(a.nsplit) * a.Hkv * a.B * a.T;
-  return launch_pdl(attn_simt_kernel<T, HD, G, FUSED>, static_cast<unsigned>(nblk), kNW * 32, C::SMEM_B, s, a);
+  if (nblk <= sm_count()) return launch_simt_hgfw<T, HD, G, FUSED, 8>(a, nblk, s);
+  return launch_simt_hgfw<T, HD, G, FUSED, 4>(a, nblk, s);
 }
 
 template <typename T, int HD, int G>

@@ -94,5 +94,6 @@ struct DecodePlan {
   size_t ws_bytes;
 };
 DecodePlan decode_plan(int sliding, int window, int hd, int H, int Hkv, int B, int max_seq_len);
+int sm_count();  // SMs of the current device
 
 }  // namespace g4

@@ -234,30 +234,39 @@ __device__ __forceinline__ DF reduce_angle_df(int p, float f, int& quadrant) {
   return r;
 }
 
-// cos and sin of p * f in double-float (absolute error about 2^-47).
-__device__ __forceinline__ void sincos_df(int p, float f, DF& c_out, DF& s_out) {
-  int quadrant;
-  const DF r = reduce_angle_df(p, f, quadrant);
-  // Taylor polynomials on |r| <= pi/4 (+ a rounding of k): the leading
-  // coefficients 1/n! in double-float, the tail (< 2^-30 of the result) in float.
-  const DF z = df_mul(r, r);
+// The two polynomials of sincos_df on the reduced angle r (z = r^2):
+// sin r = r + r z S(z) and cos r = 1 - z/2 + z^2 C(z), with the Taylor
+// coefficients 1/n! in double-float and the tail (< 2^-30 of the result) in float.
+__device__ __forceinline__ DF sin_poly_df(DF r, DF z) {
   const float zh = z.h;
-  // sin r = r + r z S(z), S(z) = -1/3! + z/5! - z^2/7! + z^3/9! - z^4/11! + z^5/13! - z^6/15!
+  // S(z) = -1/3! + z/5! - z^2/7! + z^3/9! - z^4/11! + z^5/13! - z^6/15!
   float ts = fmaf(zh, -0x1.ae7f3ep-41f, 0x1.612462p-33f);
   ts = fmaf(zh, ts, -0x1.ae6456p-26f);
   DF S = df_add(df_mul_f(z, ts), DF{0x1.71de3ap-19f, 0x1.55b1ccp-45f});
   S = df_add(df_mul(z, S), DF{-0x1.a01a02p-13f, 0x1.7f97fap-39f});
   S = df_add(df_mul(z, S), DF{0x1.111112p-7f, -0x1.dddddep-32f});
   S = df_add(df_mul(z, S), DF{-0x1.555556p-3f, 0x1.555556p-28f});
-  const DF sn = df_add(r, df_mul(df_mul(r, z), S));
-  // cos r = 1 - z/2 + z^2 C(z), C(z) = 1/4! - z/6! + z^2/8! - z^3/10! + z^4/12! - z^5/14! + z^6/16!
+  return df_add(r, df_mul(df_mul(r, z), S));
+}
+__device__ __forceinline__ DF cos_poly_df(DF z) {
+  const float zh = z.h;
+  // C(z) = 1/4! - z/6! + z^2/8! - z^3/10! + z^4/12! - z^5/14! + z^6/16!
   float tc = fmaf(zh, 0x1.ae7f3ep-45f, -0x1.93974ap-37f);
   tc = fmaf(zh, tc, 0x1.1eed8ep-29f);
   DF Cz = df_add(df_mul_f(z, tc), DF{-0x1.27e4fcp-22f, 0x1.10ec14p-47f});
   Cz = df_add(df_mul(z, Cz), DF{0x1.a01a02p-16f, -0x1.7f97fap-42f});
   Cz = df_add(df_mul(z, Cz), DF{-0x1.6c16c2p-10f, 0x1.27d27ep-35f});
   Cz = df_add(df_mul(z, Cz), DF{0x1.555556p-5f, -0x1.555556p-30f});
-  const DF cs = df_add(df_add_f(DF{-0.5f * z.h, -0.5f * z.l}, 1.0f), df_mul(df_mul(z, z), Cz));
+  return df_add(df_add_f(DF{-0.5f * z.h, -0.5f * z.l}, 1.0f), df_mul(df_mul(z, z), Cz));
+}
+
+// cos and sin of p * f in double-float (absolute error about 2^-47).
+__device__ __forceinline__ void sincos_df(int p, float f, DF& c_out, DF& s_out) {
+  int quadrant;
+  const DF r = reduce_angle_df(p, f, quadrant);
+  const DF z = df_mul(r, r);
+  const DF sn = sin_poly_df(r, z);
+  const DF cs = cos_poly_df(z);
   // theta = k pi/2 + r
   switch (quadrant) {
     case 0: c_out = cs; s_out = sn; break;
@@ -265,6 +274,21 @@ __device__ __forceinline__ void sincos_df(int p, float f, DF& c_out, DF& s_out) 
     case 2: c_out = df_neg(cs); s_out = df_neg(sn); break;
     default: c_out = sn; s_out = df_neg(cs); break;
   }
+}
+
+// Half of sincos_df, for two threads sharing one angle: part 0 evaluates the
+// cosine polynomial, part 1 the sine one; the result is cos (p f) when
+// to_cos is set on return, else sin (p f).  Same values as sincos_df.
+__device__ __forceinline__ DF sincos_df_part(int p, float f, int part, bool& to_cos) {
+  int quadrant;
+  const DF r = reduce_angle_df(p, f, quadrant);
+  const DF z = df_mul(r, r);
+  const DF v = part == 0 ? cos_poly_df(z) : sin_poly_df(r, z);
+  // cos poly: cos for quadrants 0 (+), 2 (-); sin for 1 (+), 3 (-).
+  // sin poly: sin for quadrants 0 (+), 2 (-); cos for 1 (-), 3 (+).
+  to_cos = (part == 0) == ((quadrant & 1) == 0);
+  const bool neg = part == 0 ? quadrant >= 2 : (quadrant == 1 || quadrant == 2);
+  return neg ? df_neg(v) : v;
 }
 
 // Error of a double-float table's float part: at most u (+ 2^-47).
@@ -286,19 +310,21 @@ static __device__ __noinline__ float normrope_exact_bf16(float x_self, float w_s
 
 // Float32 evaluation of one pair (lower a = element j, upper b = element
 // j + hd/2) with row inverse rms r, cos / sin c, s.  Sets need_a / need_b
-// when the float32 value cannot decide the bf16 rounding; err_y and err_rot
-// are the bounds (already multiplied by u and a safety margin) for an
-// unrotated output (times |y|) and a rotated one (times |y_a| + |y_b|).
+// when the float32 value cannot decide the bf16 rounding.  Bounds: err_y |y|
+// for an unrotated output; err_ab (|ya| + |yb|) + err_o |o| for a rotated one
+// (normrope_err_pair, normrope_err_out).
 __device__ __forceinline__ void normrope_pair_fast(float xa, float wa, float xb, float wb, float r, bool rot, float c,
-                                                   float s, float err_y, float err_rot, float& oa, float& ob,
-                                                   bool& need_a, bool& need_b) {
+                                                   float s, float err_y, float err_ab, float err_o, float& oa,
+                                                   float& ob, bool& need_a, bool& need_b) {
   const float ya = (xa * r) * wa;
   const float yb = (xb * r) * wb;
   float ea, eb;
   if (rot) {
     oa = fmaf(ya, c, -(yb * s));
     ob = fmaf(yb, c, ya * s);
-    ea = eb = err_rot * (fabsf(ya) + fabsf(yb));
+    const float shared = err_ab * (fabsf(ya) + fabsf(yb));
+    ea = fmaf(err_o, fabsf(oa), shared);
+    eb = fmaf(err_o, fabsf(ob), shared);
   } else {
     oa = ya;
     ob = yb;
