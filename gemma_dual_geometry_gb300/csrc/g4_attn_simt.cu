@@ -167,7 +167,8 @@ __device__ __forceinline__ float through(float x) {
 }
 
 // RMSNorm (optional weight) then rotate_half RoPE of one row held in the lane
-// layout above (src: the same row in memory), at position pos; the partner
+// layout above (src: the same row in memory; wf: the lane's weights, from w,
+// or ones when w is null), at position pos; the partner
 // of element d is d +- HD/2, which is the same lane (NPC >= 2) or lane ^ 16
 // (NPC == 1).  bf16 results are the correctly rounded real values
 // (g4_normrope.cuh), the ones the append kernel stores, decided in three
@@ -176,8 +177,8 @@ __device__ __forceinline__ float through(float x) {
 // double-float inverse rms for the rest.  s_cos / s_sin hold cos and sin of
 // the HD/2 pairs.
 template <typename T, int HD, int NPC, int PE>
-__device__ __forceinline__ void norm_rope_row(float* f, const T* src, const float* w, bool rope, const DF* s_cos,
-                                              const DF* s_sin, int n_rot, float eps, int lane) {
+__device__ __forceinline__ void norm_rope_row(float* f, const float* wf, const T* src, const float* w, bool rope,
+                                              const DF* s_cos, const DF* s_sin, int n_rot, float eps, int lane) {
   constexpr int EL = NPC * PE;
   constexpr bool kBF16 = sizeof(T) == 2;
   constexpr float kErrY = normrope_err_y<EL>();
@@ -186,13 +187,6 @@ __device__ __forceinline__ void norm_rope_row(float* f, const T* src, const floa
   constexpr float kErrR = normrope_err_r<EL>();
   const float sf = row_sumsq_f32<EL>(f);
   const float r = inv_rms_f32(sf, HD, eps);
-  float wf[EL];
-  if (w != nullptr) {
-    load_row<float, NPC, PE>(w, lane, wf);
-  } else {
-#pragma unroll
-    for (int i = 0; i < EL; ++i) wf[i] = 1.0f;
-  }
   // raw partner values and weights
   float fp[EL], wp[EL];
   if constexpr (NPC >= 2) {
@@ -371,6 +365,42 @@ __global__ void __launch_bounds__(NW * 32, (SimtCfg<T, HD, G, NW>::MINB))
     // L-1 the new k and v -- normed and roped, one row per warp, into shared
     // memory (k and v also into the cache row L-1).
     const int pos = L - 1;
+    const int njobs = G + (new_key ? 2 : 0);
+    // Row `job` of the jobs: q head job (< G), then the new k and v.
+    struct Job {
+      const T* src;
+      T* dst_g;
+      const float* w;
+      bool rope;
+    };
+    auto job_of = [&](int job) -> Job {
+      Job j;
+      if (job < G) {
+        j.src = static_cast<const T*>(a.q) + (static_cast<size_t>(bt) * a.H + kvh * G + job) * HD;
+        j.dst_g = nullptr;
+        j.w = a.q_w;
+        j.rope = true;
+      } else {
+        const bool is_k = job == G;
+        j.src = static_cast<const T*>(is_k ? a.k_raw : a.v_raw) + (static_cast<size_t>(b) * a.Hkv + kvh) * HD;
+        j.dst_g = static_cast<T*>(is_k ? a.cache_k : a.cache_v) + (head_base + (L - 1)) * HD;
+        j.w = is_k ? a.k_w : nullptr;
+        j.rope = is_k;
+      }
+      return j;
+    };
+    auto load_job = [&](const Job& j, float* f, float* wf) {
+      load_row<T, C::NPC, C::PE>(j.src, lane, f);
+      if (j.w != nullptr) {
+        load_row<float, C::NPC, C::PE>(j.w, lane, wf);
+      } else {
+#pragma unroll
+        for (int i = 0; i < C::EL; ++i) wf[i] = 1.0f;
+      }
+    };
+    // The warp's first row is loaded before the table is built, so the two overlap.
+    float f[C::EL], wf[C::EL];
+    if (warp < njobs) load_job(job_of(warp), f, wf);
     for (int idx = threadIdx.x; idx < HD; idx += blockDim.x) {
       const int j = idx >> 1, part = idx & 1;
       if (j < a.n_rot) {
@@ -386,28 +416,12 @@ __global__ void __launch_bounds__(NW * 32, (SimtCfg<T, HD, G, NW>::MINB))
     __syncthreads();
     T* s_qn = reinterpret_cast<T*>(smem + C::QN_OFF);
     T* s_kn = reinterpret_cast<T*>(smem + C::KN_OFF);
-    const int njobs = G + (new_key ? 2 : 0);
     for (int job = warp; job < njobs; job += NW) {
-      const T* src;
-      T* dst_g = nullptr;
-      const float* wgt = a.q_w;
-      bool rope = true;
-      if (job < G) {
-        src = static_cast<const T*>(a.q) + (static_cast<size_t>(bt) * a.H + kvh * G + job) * HD;
-      } else {
-        const size_t raw = (static_cast<size_t>(b) * a.Hkv + kvh) * HD;
-        const size_t row = (head_base + (L - 1)) * HD;
-        const bool is_k = job == G;
-        src = static_cast<const T*>(is_k ? a.k_raw : a.v_raw) + raw;
-        dst_g = static_cast<T*>(is_k ? a.cache_k : a.cache_v) + row;
-        wgt = is_k ? a.k_w : nullptr;
-        rope = is_k;
-      }
-      float f[C::EL];
-      load_row<T, C::NPC, C::PE>(src, lane, f);
-      norm_rope_row<T, HD, C::NPC, C::PE>(f, src, wgt, rope, s_cos, s_sin, a.n_rot, a.eps, lane);
+      const Job j = job_of(job);
+      if (job != warp) load_job(j, f, wf);
+      norm_rope_row<T, HD, C::NPC, C::PE>(f, wf, j.src, j.w, j.rope, s_cos, s_sin, a.n_rot, a.eps, lane);
       store_row<T, C::NPC, C::PE>(job < G ? s_qn + job * HD : s_kn + (job - G) * HD, lane, f);
-      if (dst_g != nullptr) store_row<T, C::NPC, C::PE>(dst_g, lane, f);
+      if (j.dst_g != nullptr) store_row<T, C::NPC, C::PE>(j.dst_g, lane, f);
     }
     __syncthreads();
   }
@@ -633,72 +647,121 @@ __global__ void __launch_bounds__(NW * 32, (SimtCfg<T, HD, G, NW>::MINB))
   __syncthreads();
   if (*s_flag == 0) return;
   __threadfence();
-  for (int h = warp; h < G; h += NW) {
-    const size_t p0 = (static_cast<size_t>(bt) * a.H + kvh * G + h) * a.nsplit;
-    float M = -INFINITY;
-    for (int s = lane; s < a.nsplit; s += 32) M = fmaxf(M, __ldcg(a.ws_m + p0 + s));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float Ls = 0.0f;
-    for (int s = lane; s < a.nsplit; s += 32) {
-      const float ms_ = __ldcg(a.ws_m + p0 + s);
-      const float w = (ms_ == -INFINITY) ? 0.0f : exp2f(ms_ - M);
-      s_w[h * kMaxSplits + s] = w;
-      Ls += w * __ldcg(a.ws_l + p0 + s);
-    }
-    Ls = warp_sum(Ls);
-    const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
-    __syncwarp();
-    for (int s = lane; s < a.nsplit; s += 32) s_w[h * kMaxSplits + s] *= inv;
-  }
-  __syncthreads();
-  // Each thread owns float4 groups of the G*HD outputs and keeps many loads in
-  // flight: 8 splits x up to 4 groups per round.
-  constexpr int NG4 = G * HD / 4;                        // float4 groups
-  constexpr int PER = (NG4 + NW * 32 - 1) / (NW * 32);  // groups per thread
-  float4 acc[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) acc[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  const size_t pbase = (static_cast<size_t>(bt) * a.H + kvh * G) * a.nsplit;
-  for (int s0 = 0; s0 < a.nsplit; s0 += 8) {
-    float4 v[PER][8];
+  if (a.nsplit <= 8) {
+    // Each thread owns float4 groups of the G*HD outputs and merges the (at
+    // most 8) splits with log-sum-exp weights, all of its loads -- running
+    // maxima, denominators and partial outputs -- in flight at once.
+    constexpr int NG4 = G * HD / 4;                        // float4 groups
+    constexpr int PER = (NG4 + NW * 32 - 1) / (NW * 32);  // groups per thread
+    const size_t pbase = (static_cast<size_t>(bt) * a.H + kvh * G) * a.nsplit;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int g4i = threadIdx.x + i * NW * 32;
+      if (g4i >= NG4) break;
       const int h = (g4i * 4) / HD;
       const int d = (g4i * 4) % HD;
+      const size_t prow = pbase + static_cast<size_t>(h) * a.nsplit;  // (head h, split 0)
+      float mv[8], lv[8];
+      float4 ov[8];
+      float M = -INFINITY;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int sp = s0 + u;
-        v[i][u] = (g4i < NG4 && sp < a.nsplit)
-                      ? __ldcg(reinterpret_cast<const float4*>(a.ws_o + ((pbase + static_cast<size_t>(h) * a.nsplit +
-                                                                           sp) * HD + d)))
-                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        mv[u] = -INFINITY;
+        if (u < a.nsplit) {
+          mv[u] = __ldcg(a.ws_m + prow + u);
+          lv[u] = __ldcg(a.ws_l + prow + u);
+          ov[u] = __ldcg(reinterpret_cast<const float4*>(a.ws_o + (prow + u) * HD + d));
+        }
+        M = fmaxf(M, mv[u]);
       }
-    }
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      const int g4i = threadIdx.x + i * NW * 32;
-      const int h = g4i < NG4 ? (g4i * 4) / HD : 0;
+      float Ls = 0.0f;
+      float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const float w = (s0 + u < a.nsplit) ? s_w[h * kMaxSplits + s0 + u] : 0.0f;
-        acc[i].x = fmaf(w, v[i][u].x, acc[i].x);
-        acc[i].y = fmaf(w, v[i][u].y, acc[i].y);
-        acc[i].z = fmaf(w, v[i][u].z, acc[i].z);
-        acc[i].w = fmaf(w, v[i][u].w, acc[i].w);
+        if (mv[u] != -INFINITY) {
+          const float w = exp2f(mv[u] - M);
+          Ls = fmaf(w, lv[u], Ls);
+          acc.x = fmaf(w, ov[u].x, acc.x);
+          acc.y = fmaf(w, ov[u].y, acc.y);
+          acc.z = fmaf(w, ov[u].z, acc.z);
+          acc.w = fmaf(w, ov[u].w, acc.w);
+        }
       }
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int g4i = threadIdx.x + i * NW * 32;
-    if (g4i < NG4) {
-      const int h = (g4i * 4) / HD;
-      const int d = (g4i * 4) % HD;
+      const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
       T* dst = static_cast<T*>(a.out) + (static_cast<size_t>(bt) * a.H + kvh * G + h) * HD + d;
-      const float f[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
+      const float f[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
       store_elems<4>(dst, f);
+    }
+  } else {
+    // More splits: the log-sum-exp weights per head first (into shared
+    // memory), then every partial output load of a round in flight.
+    for (int h = warp; h < G; h += NW) {
+      const size_t p0 = (static_cast<size_t>(bt) * a.H + kvh * G + h) * a.nsplit;
+      float M = -INFINITY;
+      for (int s = lane; s < a.nsplit; s += 32) M = fmaxf(M, __ldcg(a.ws_m + p0 + s));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float Ls = 0.0f;
+      for (int s = lane; s < a.nsplit; s += 32) {
+        const float ms_ = __ldcg(a.ws_m + p0 + s);
+        const float w = (ms_ == -INFINITY) ? 0.0f : exp2f(ms_ - M);
+        s_w[h * kMaxSplits + s] = w;
+        Ls += w * __ldcg(a.ws_l + p0 + s);
+      }
+      Ls = warp_sum(Ls);
+      const float inv = Ls > 0.0f ? 1.0f / Ls : 0.0f;
+      __syncwarp();
+      for (int s = lane; s < a.nsplit; s += 32) s_w[h * kMaxSplits + s] *= inv;
+    }
+    __syncthreads();
+    // Each thread owns float4 groups of the G*HD outputs and keeps many loads in
+    // flight: 8 splits x up to 4 groups per round.
+    constexpr int NG4 = G * HD / 4;                        // float4 groups
+    constexpr int PER = (NG4 + NW * 32 - 1) / (NW * 32);  // groups per thread
+    float4 acc[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    const size_t pbase = (static_cast<size_t>(bt) * a.H + kvh * G) * a.nsplit;
+    for (int s0 = 0; s0 < a.nsplit; s0 += 8) {
+      float4 v[PER][8];
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int g4i = threadIdx.x + i * NW * 32;
+        const int h = (g4i * 4) / HD;
+        const int d = (g4i * 4) % HD;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int sp = s0 + u;
+          v[i][u] = (g4i < NG4 && sp < a.nsplit)
+                        ? __ldcg(reinterpret_cast<const float4*>(a.ws_o + ((pbase + static_cast<size_t>(h) * a.nsplit +
+                                                                             sp) * HD + d)))
+                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const int g4i = threadIdx.x + i * NW * 32;
+        const int h = g4i < NG4 ? (g4i * 4) / HD : 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float w = (s0 + u < a.nsplit) ? s_w[h * kMaxSplits + s0 + u] : 0.0f;
+          acc[i].x = fmaf(w, v[i][u].x, acc[i].x);
+          acc[i].y = fmaf(w, v[i][u].y, acc[i].y);
+          acc[i].z = fmaf(w, v[i][u].z, acc[i].z);
+          acc[i].w = fmaf(w, v[i][u].w, acc[i].w);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int g4i = threadIdx.x + i * NW * 32;
+      if (g4i < NG4) {
+        const int h = (g4i * 4) / HD;
+        const int d = (g4i * 4) % HD;
+        T* dst = static_cast<T*>(a.out) + (static_cast<size_t>(bt) * a.H + kvh * G + h) * HD + d;
+        const float f[4] = {acc[i].x, acc[i].y, acc[i].z, acc[i].w};
+        store_elems<4>(dst, f);
+      }
     }
   }
   if (threadIdx.x == 0) *ticket = 0u;  // ready for the next call
