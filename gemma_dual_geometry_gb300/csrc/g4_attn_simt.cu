@@ -877,6 +877,13 @@ DecodePlan decode_plan(int sliding, int window, int hd, int H, int Hkv, int B, i
   if (cap > kMaxSplits) cap = kMaxSplits;
   if (cap < 1) cap = 1;
   int nsplit = 0;
+  if (units * 2 <= sm_count()) {
+    // Few (row, kv head) units: one 8-warp CTA per SM, as many splits as fit
+    // one wave, so each CTA streams a long key range and the per-CTA work
+    // (norm, merges) is paid as few times as possible.
+    nsplit = sm_count() / units;
+    if (nsplit > cap) nsplit = cap;
+  }
   for (int m = 4; m >= 1 && nsplit == 0; --m) {
     const int ns = static_cast<int>((static_cast<long long>(m) * slots) / units);
     if (ns >= 1 && ns <= cap) nsplit = ns;

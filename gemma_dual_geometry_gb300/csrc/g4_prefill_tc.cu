@@ -124,16 +124,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
   pdl_trigger();
 
-  // Block -> (q tile, sequence, head, output half); heaviest (last) tiles first.
+  // Block -> (output half, q head of the group, q tile, kv head, sequence):
+  // the CTAs running together share one (sequence, kv head), so its K / V
+  // stay in L2 while they stream them; within it the heaviest (last) tiles go first.
   const int nqt = (a.T + kBM - 1) / kBM;
+  const int grp = a.H / a.Hkv;
   int idx = blockIdx.x;
   const int dh = idx % C::NDH;
   idx /= C::NDH;
-  const int h = idx % a.H;
-  idx /= a.H;
-  const int b = idx % a.B;
-  const int qt = nqt - 1 - idx / a.B;
-  const int kvh = h / (a.H / a.Hkv);
+  const int hq = idx % grp;
+  idx /= grp;
+  const int qt = nqt - 1 - idx % nqt;
+  idx /= nqt;
+  const int kvh = idx % a.Hkv;
+  const int b = idx / a.Hkv;
+  const int h = kvh * grp + hq;
 
   const int q_start = a.q_start[b];
   const int q0 = qt * kBM;
