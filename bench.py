@@ -42,6 +42,10 @@ METRIC = "prefill attn tokens/s and decode KV GB/s vs GB300 roofline, 1 GPU"
 WORKLOAD = "stack42_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DECODE_EVENT_STEPS = (0, 32, 64, 96, 127)
+# DRAM bytes (read + write) per launch from one ncu capture of each kernel on
+# the 42-layer stack (profiles/*_stack42_bf16.md: dram__bytes.sum.per_second x
+# gpu__time_duration); the decode figures are for the first decode step.
+PROFILED_TRAFFIC = {"prefill_full": 637000448, "decode_full": 137844493, "decode_sliding": 8491776}
 
 
 def parse_args(argv=None):
@@ -389,7 +393,8 @@ def run_ours(args, cfg):
                       achieved=pf_flops / pf_avg / 1e12, peak=peaks["bf16_tflops_sustained"], unit="TFLOP/s",
                       peak_kind=f"{peak_src} bf16 dense, sustained (timed inside a long step)",
                       flops_per_launch=pf_flops, avg_launch_ms=pf_avg * 1e3, launches_sampled=len(pf_launch),
-                      launches_per_step=len(job.full_layers), traffic=None)
+                      launches_per_step=len(job.full_layers), traffic=PROFILED_TRAFFIC["prefill_full"],
+                      traffic_source="profiles/prefill_tc_full512_stack42_bf16.md")
     rl_prefill["frac"] = rl_prefill["achieved"] / rl_prefill["peak"]
     rooflines = [rl_prefill]
     kinds = (("full", job.full_layers, "attn_simt_kernel<bf16,512,4,fused> (full-layer decode step: append + "
@@ -407,7 +412,10 @@ def run_ours(args, cfg):
                       achieved=avg_b / avg_t / 1e9, peak=peaks["hbm_gbs"], unit="GB/s",
                       peak_kind=f"{peak_src} HBM copy bandwidth", bytes_per_launch=avg_b,
                       avg_launch_ms=avg_t * 1e3, launches_sampled=len(samples),
-                      launches_per_step=len(layers) * cfg["decode_steps"], traffic=None,
+                      launches_per_step=len(layers) * cfg["decode_steps"],
+                      traffic=PROFILED_TRAFFIC["decode_" + kind],
+                      traffic_source=f"profiles/decode_step_{'full512' if kind == 'full' else 'sliding256'}"
+                                     "_stack42_bf16.md (first decode step)",
                       per_launch_gbs_min=min(per) / 1e9, per_launch_gbs_max=max(per) / 1e9)
         rl_dec["frac"] = rl_dec["achieved"] / rl_dec["peak"]
         if kind == "sliding":
