@@ -305,8 +305,14 @@ __global__ void __launch_bounds__(NW * 32, (SimtCfg<T, HD, G, NW>::MINB))
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   uint64_t* wbar = bars + warp * C::NST;
-  if (lane == 0) {
-    for (int i = 0; i < C::NST; ++i) mbar_init(smem_u32(&wbar[i]), 1);
+  // With 8 warps and 1 KB rows the last warp (which has no norm row when
+  // G <= 6) sets up every warp's stage barriers and issues their first stages
+  // (48 copies, which take microseconds to issue), so the others go straight
+  // to the cos/sin table; they first touch the barriers after the CTA barrier
+  // that ends the table.  Otherwise each warp does its own.
+  constexpr bool kIssuer = NW > 4 && HD >= 512;
+  if (kIssuer ? (warp == NW - 1 && lane == 0) : lane == 0) {
+    for (int i = 0; i < (kIssuer ? NW : 1) * C::NST; ++i) mbar_init(smem_u32(&(kIssuer ? bars : wbar)[i]), 1);
     fence_mbar_init();
   }
   __syncwarp();
@@ -342,22 +348,29 @@ __global__ void __launch_bounds__(NW * 32, (SimtCfg<T, HD, G, NW>::MINB))
   const T* gk = static_cast<const T*>(a.ck) + head_base * HD;
   const T* gv = static_cast<const T*>(a.cv) + head_base * HD;
 
-  auto issue = [&](int st_idx, int buf) {
+  // stage st_idx of warp w's ring into its buffer buf
+  auto issue_for = [&](int w, int st_idx, int buf) {
     const int kk0 = k0 + st_idx * C::SK;
     const int n = min(C::SK, k1c - kk0);
     const uint32_t bytes = static_cast<uint32_t>(n) * C::ROWB;
-    const uint32_t bar = smem_u32(&wbar[buf]);
+    const uint32_t bar = smem_u32(&bars[w * C::NST + buf]);
+    uint8_t* rw = smem + w * (C::NST * 2 * C::STAGE_B);
     mbar_arrive_expect_tx(bar, 2 * bytes);
-    bulk_g2s(smem_u32(ring + buf * 2 * C::STAGE_B), gk + static_cast<size_t>(kk0) * HD, bytes, bar);
-    bulk_g2s(smem_u32(ring + buf * 2 * C::STAGE_B + C::STAGE_B), gv + static_cast<size_t>(kk0) * HD, bytes, bar);
+    bulk_g2s(smem_u32(rw + buf * 2 * C::STAGE_B), gk + static_cast<size_t>(kk0) * HD, bytes, bar);
+    bulk_g2s(smem_u32(rw + buf * 2 * C::STAGE_B + C::STAGE_B), gv + static_cast<size_t>(kk0) * HD, bytes, bar);
   };
+  auto issue = [&](int st_idx, int buf) { issue_for(warp, st_idx, buf); };
 
-  if (lane == 0) {
+  // (lane w of the issuing warp issues warp w's stages)
+  if (kIssuer ? (warp == NW - 1 && lane < NW) : lane == 0) {
+    const int w = kIssuer ? lane : warp;
     for (int i = 0; i < C::NST; ++i) {
-      const int st = warp + i * NW;
-      if (st < nstages) issue(st, i);
+      const int st = w + i * NW;
+      if (st < nstages) issue_for(w, st, i);
     }
   }
+  // (the fused step's table ends with a CTA barrier; the plain one needs its own)
+  if constexpr (kIssuer && !FUSED) __syncthreads();
 
   if constexpr (FUSED) {
     // cos/sin of the new token's position (two threads per rotated pair, one
@@ -401,7 +414,8 @@ __global__ void __launch_bounds__(NW * 32, (SimtCfg<T, HD, G, NW>::MINB))
     // The warp's first row is loaded before the table is built, so the two overlap.
     float f[C::EL], wf[C::EL];
     if (warp < njobs) load_job(job_of(warp), f, wf);
-    for (int idx = threadIdx.x; idx < HD; idx += blockDim.x) {
+    constexpr int kTableThreads = (kIssuer ? NW - 1 : NW) * 32;
+    for (int idx = threadIdx.x; idx < HD && threadIdx.x < kTableThreads; idx += kTableThreads) {
       const int j = idx >> 1, part = idx & 1;
       if (j < a.n_rot) {
         bool to_cos;
