@@ -9,11 +9,16 @@
 // One CTA computes a 128-query-row tile of one (sequence, head) and, for
 // head_dim 512, one 256-wide half of the output columns (two CTAs per tile
 // then recompute the same scores; TMEM holds 512 f32 columns per SM and a
-// 128 x 512 accumulator alone would fill it).  Warp roles (192 threads):
-//   warp 0      TMA producer: the Q tile once, then K chunks (128 keys x 64
-//               dims) and V chunks (VK keys x DV dims) through a ring of
-//               16 KB shared-memory slots, 128-byte swizzled.
-//   warp 1      allocates TMEM and issues tcgen05.mma (one elected lane):
+// 128 x 512 accumulator alone would fill it).  CTAs run in (sequence, kv head)
+// groups, heaviest query tiles first, so the CTAs in flight share their K / V
+// in L2.  Warp roles (320 threads):
+//   warp 0      TMA producer (one lane): the Q tile, then K parts (128 keys x
+//               64..256 dims) and V parts (64..128 keys x DV dims) as 5-D
+//               boxes, one request per 32-64 KB (a request costs the SM about
+//               the same whatever its size), through a ring of slots,
+//               128-byte swizzled.
+//   warp 1      allocates TMEM; one lane issues every tcgen05.mma from
+//               precomputed descriptors:
 //                 S[j%2] = Q K_j^T      (M=128, N=128, K=head_dim; A, B from
 //                                        shared memory, K-major)
 //                 O     += P_j V_j      (M=128, N=DV,  K=128; A = P_j from
@@ -24,16 +29,18 @@
 //               touch its quarter's 32 lanes), each thread half a query row
 //               (64 of the 128 score columns; TMEM lane = row): load the
 //               whole S row with tcgen05.ld (both threads of a row find the
-//               same maximum), mask (causal / window / keys past the cache),
-//               online softmax in the log2 domain with the running maximum
-//               raised only when it grows by more than 2^64 (the stale
-//               maximum is exact for O / l), rescale its half of the O row in
-//               TMEM when it is raised, and write its P half as bf16 over the
-//               S buffer (packed: 32 columns); finally its half of O / l to
-//               global memory (the two halves' row sums meet in shared
-//               memory once, at the end).  The row sum l adds the bf16-rounded P values, the
-//               weights the PV MMA really applies, so a row dominated by one
-//               key returns that key's value without the rounding error of P.
+//               same maximum), mask (one visible key interval per row:
+//               causal end, window start, keys past the cache), online
+//               softmax in the log2 domain with the running maximum raised
+//               only when it grows by more than 2^64 (the stale maximum is
+//               exact for O / l), rescale its half of the O row in TMEM when
+//               it is raised, and write its P half as bf16 over the S buffer
+//               (packed: 32 columns).  The row sum l adds the bf16-rounded P
+//               values, the weights the PV MMA really applies, so a row
+//               dominated by one key returns that key's value without the
+//               rounding error of P; the two halves' sums meet in shared
+//               memory once, at the end.  Epilogue: O / l as bf16 into the Q
+//               area (swizzled like the output tensor map), one TMA store.
 // TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O [256, 256 + DV).
 // The MMAs of one thread execute in issue order, so QK_{j+2} (issued after
 // PV_j) overwrites P_j only after PV_j has read it; no barrier is needed
