@@ -259,8 +259,10 @@ __device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, uint32_t sr
 
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
-// Waits until the bulk stores committed so far have completed (written to global memory).
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Waits until the bulk stores committed so far have finished reading their
+// shared-memory source (the writes to global memory complete on their own and
+// are visible once the grid has completed).
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -506,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 2 && lane == 0 && ntiles > 0 && !*abort) {
       tma_store_5d(&tm_o, sQ, 0, q0, dh * (C::DV / 64), h, b);
       bulk_commit_group();
-      bulk_wait_all();
+      bulk_wait_read_all();  // the tile's shared memory must outlive the copy's reads
     }
   }
 
