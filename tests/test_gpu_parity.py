@@ -149,8 +149,8 @@ PREFILL_CASES = [
     (W.F32, F, 128, 0, 2, 90, [0, 11]),
     (W.F32, F, 512, 0, 1, 50, [3]),
     (W.F32, S, 256, 7, 1, 40, [0]),
-    # more work items (query tile x head x output half) than a GB300 has SMs:
-    # the persistent prefill CTAs each take several, of different lengths
+    # more work items (query tile x head x output half) than a GB300 has SMs,
+    # ragged lengths and query offsets in one launch
     (W.BF16, S, 256, 512, 4, 1000, [0, 37, 500, 1024]),
     (W.BF16, F, 512, 0, 3, 700, [0, 300, 1111]),
 ]
