@@ -6,12 +6,15 @@
 // over keys j <= i (and i - j < window on sliding layers), query head h
 // reading kv head h / (H / Hkv).
 //
-// One CTA computes a 128-query-row tile of one (sequence, head) and, for
-// head_dim 512, one 256-wide half of the output columns (two CTAs per tile
+// A work item is a 128-query-row tile of one (sequence, head) and, for
+// head_dim 512, one 256-wide half of the output columns (two items per tile
 // then recompute the same scores; TMEM holds 512 f32 columns per SM and a
-// 128 x 512 accumulator alone would fill it).  CTAs run in (sequence, kv head)
-// groups, heaviest query tiles first, so the CTAs in flight share their K / V
-// in L2.  Warp roles (320 threads):
+// 128 x 512 accumulator alone would fill it).  Items run in (sequence, kv
+// head) groups, heaviest query tiles first, so the CTAs in flight share their
+// K / V in L2.  The kernel is persistent: one CTA per SM takes items
+// blockIdx.x, blockIdx.x + gridDim.x, ..., with its barriers, ring and TMEM
+// running on from item to item, so the next item's Q and first K parts load
+// while the current one finishes.  Warp roles (320 threads):
 //   warp 0      TMA producer (one lane): the Q tile, then K parts (128 keys x
 //               64..256 dims) and V parts (64..128 keys x DV dims) as 5-D
 //               boxes, one request per 32-64 KB (a request costs the SM about
@@ -39,8 +42,9 @@
 //               values, the weights the PV MMA really applies, so a row
 //               dominated by one key returns that key's value without the
 //               rounding error of P; the two halves' sums meet in shared
-//               memory once, at the end.  Epilogue: O / l as bf16 into the Q
-//               area (swizzled like the output tensor map), one TMA store.
+//               memory once, at the end.  Epilogue: O / l as bf16 into the
+//               ring slots of the item's last V parts (swizzled like the
+//               output tensor map), TMA stores, then those slots are freed.
 // TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O [256, 256 + DV).
 // The MMAs of one thread execute in issue order, so QK_{j+2} (issued after
 // PV_j) overwrites P_j only after PV_j has read it; no barrier is needed
@@ -81,6 +85,10 @@ struct TcCfg {
   static constexpr int VPARTS = kBN / VKP;
   static constexpr int VPB = VKP * DV * 2;          // V part bytes
   static constexpr int SLOTB = KPB > VPB ? KPB : VPB;
+  // The output tile (DV / 64 chunks) is staged in the slots of the last V
+  // parts of the item: CPS chunks per slot, OSLOTS slots.
+  static constexpr int CPS = SLOTB / kChunkB;
+  static constexpr int OSLOTS = (DV / 64) / CPS;
   static constexpr int Q_OFF = 0;
   static constexpr int RING_OFF = Q_OFF + QCH * kChunkB;
   static constexpr int BAR_B = 3072;
@@ -91,15 +99,20 @@ struct TcCfg {
   static_assert(NSLOT >= 2, "ring depth");
   static_assert(SMEM_B <= kSmemMax, "shared memory budget");
   static_assert(VKP % 16 == 0 && kBN % VKP == 0 && QCH % KPARTS == 0, "tiling");
+  static_assert(SLOTB % kChunkB == 0 && (DV / 64) % CPS == 0 && OSLOTS >= 1 && OSLOTS <= VPARTS &&
+                    OSLOTS < NSLOT && VPB == SLOTB,
+                "output staging in the ring");
 };
 
 struct TcBars {
-  uint64_t q_full;
+  uint64_t q_full;     // the current item's Q tile has landed (one phase per item)
+  uint64_t q_free;     // every QK MMA of the current item is complete (Q may be replaced)
   uint64_t s_full[2];  // QK_j complete (tile parity)
   uint64_t p_full[2];  // P_j written to TMEM by all 128 softmax threads
   uint64_t o_done[2];  // PV_j complete
   uint64_t drain;
   uint64_t sum_full[4];  // [lane quarter]: both row-sum shares written
+  uint64_t s_read[4];    // [lane quarter]: both warps have S_j in registers (P_j may overwrite it)
   uint64_t full[kMaxSlots];
   uint64_t empty[kMaxSlots];
   uint32_t tmem_base;
@@ -107,6 +120,57 @@ struct TcBars {
   float red[2][kBM];  // [column half][row]: row-sum shares
 };
 static_assert(sizeof(TcBars) <= 3072, "barrier block");
+
+// All 256 softmax threads meet (named barrier 1) and learn whether any of
+// them passed a nonzero flag.
+__device__ __forceinline__ bool softmax_sync_any(int flag) {
+  uint32_t any;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, 256, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(any)
+      : "r"(flag)
+      : "memory");
+  return any != 0;
+}
+
+// Work item -> (output half, q head of the group, q tile, kv head, sequence)
+// and the key tiles it needs.  Items run in (sequence, kv head) groups so the
+// CTAs working at the same time share one K / V in L2; within a group the
+// heaviest (last) query tiles come first.
+struct TcItem {
+  int dh, h, kvh, b;
+  int q0, valid_rows, qpos_first, Lk, kt_begin, ntiles;
+};
+
+template <int NDH>
+__device__ __forceinline__ TcItem tc_item(const PrefillTcArgs& a, int it, int nqt) {
+  TcItem w;
+  const int grp = a.H / a.Hkv;
+  int idx = it;
+  w.dh = idx % NDH;
+  idx /= NDH;
+  const int hq = idx % grp;
+  idx /= grp;
+  const int qt = nqt - 1 - idx % nqt;
+  idx /= nqt;
+  w.kvh = idx % a.Hkv;
+  w.b = idx / a.Hkv;
+  w.h = w.kvh * grp + hq;
+  const int q_start = a.q_start[w.b];
+  w.q0 = qt * kBM;
+  w.valid_rows = min(kBM, a.T - w.q0);
+  w.qpos_first = q_start + w.q0;
+  const int qpos_last = w.qpos_first + w.valid_rows - 1;
+  w.Lk = min(q_start + a.T, a.max_len);  // cache rows holding keys
+  const int kend = min(qpos_last + 1, w.Lk);
+  const int kbeg = a.sliding ? max(0, w.qpos_first - a.window + 1) : 0;
+  w.kt_begin = kbeg / kBN;
+  w.ntiles = max(0, (kend + kBN - 1) / kBN - w.kt_begin);
+  return w;
+}
 
 template <int HD>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -131,35 +195,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();
   pdl_trigger();
 
-  // Block -> (output half, q head of the group, q tile, kv head, sequence):
-  // the CTAs running together share one (sequence, kv head), so its K / V
-  // stay in L2 while they stream them; within it the heaviest (last) tiles go first.
   const int nqt = (a.T + kBM - 1) / kBM;
-  const int grp = a.H / a.Hkv;
-  int idx = blockIdx.x;
-  const int dh = idx % C::NDH;
-  idx /= C::NDH;
-  const int hq = idx % grp;
-  idx /= grp;
-  const int qt = nqt - 1 - idx % nqt;
-  idx /= nqt;
-  const int kvh = idx % a.Hkv;
-  const int b = idx / a.Hkv;
-  const int h = kvh * grp + hq;
-
-  const int q_start = a.q_start[b];
-  const int q0 = qt * kBM;
-  const int valid_rows = min(kBM, a.T - q0);
-  const int qpos_first = q_start + q0;
-  const int qpos_last = qpos_first + valid_rows - 1;
-  const int Lk = min(q_start + a.T, a.max_len);  // cache rows holding keys
-  const int kend = min(qpos_last + 1, Lk);
-  const int kbeg = a.sliding ? max(0, qpos_first - a.window + 1) : 0;
-  const int kt_begin = kbeg / kBN;
-  const int ntiles = max(0, (kend + kBN - 1) / kBN - kt_begin);
+  const int nitems = nqt * a.H * a.B * C::NDH;
 
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->q_full), 1);
+    mbar_init(smem_u32(&bars->q_free), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->s_full[i]), 1);
       mbar_init(smem_u32(&bars->p_full[i]), 256);
@@ -167,6 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(smem_u32(&bars->drain), 1);
     for (int qq = 0; qq < 4; ++qq) mbar_init(smem_u32(&bars->sum_full[qq]), 64);
+    for (int qq = 0; qq < 4; ++qq) mbar_init(smem_u32(&bars->s_read[qq]), 64);
     for (int i = 0; i < C::NSLOT; ++i) mbar_init(smem_u32(&bars->full[i]), 1);
     for (int i = 0; i < C::NSLOT; ++i) mbar_init(smem_u32(&bars->empty[i]), 1);
     bars->abort = 0;
@@ -185,22 +227,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // One lane issues every copy (a warp-wide wait per slot would cost more
-    // than the copy takes to issue).
-    if (lane == 0 && ntiles > 0) {
+    // than the copy takes to issue).  The ring runs on across work items: the
+    // next item's Q is loaded once the last QK MMA of the current one has
+    // read the old Q, and its first K parts go into whatever slots are free
+    // while the current item finishes.
+    if (lane == 0) {
       prefetch_tensormap(&tm_q);
       prefetch_tensormap(&tm_k);
       prefetch_tensormap(&tm_v);
       const uint32_t qb = smem_u32(&bars->q_full);
-      mbar_arrive_expect_tx(qb, C::QCH * kChunkB);
-      // Q tile: 128 rows x QCH chunks in one request (two for head_dim 512)
-      constexpr int QREQ = C::QCH > 4 ? 2 : 1;
-#pragma unroll
-      for (int r = 0; r < QREQ; ++r)
-        tma_load_5d(sQ + r * (C::QCH / QREQ) * kChunkB, &tm_q, 0, q0, r * (C::QCH / QREQ), h, b, qb);
       bool ok = true;
       int seq = 0;
       int slot = 0;        // ring slot of the next part
       uint32_t phase = 0;  // parity of that slot's current use
+      int nq = 0;          // items whose Q has been requested
       auto advance = [&]() {
         ++seq;
         if (++slot == C::NSLOT) {
@@ -208,31 +248,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           phase ^= 1u;
         }
       };
-      auto load_k = [&](int kt) {
-        for (int p2 = 0; p2 < C::KPARTS && ok; ++p2) {
-          if (!thread_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, a.err, abort)) { ok = false; break; }
-          const uint32_t fb = smem_u32(&bars->full[slot]);
-          mbar_arrive_expect_tx(fb, C::KPB);
-          tma_load_5d(sRing + slot * C::SLOTB, &tm_k, 0, kt * kBN, p2 * C::CPP, kvh, b, fb);
-          advance();
+      for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+        const TcItem w = tc_item<C::NDH>(a, it, nqt);
+        if (w.ntiles == 0) continue;
+        if (nq > 0 && !thread_wait(smem_u32(&bars->q_free), (nq - 1) & 1, a.err, abort)) break;
+        mbar_arrive_expect_tx(qb, C::QCH * kChunkB);
+        // Q tile: 128 rows x QCH chunks in one request (two for head_dim 512)
+        constexpr int QREQ = C::QCH > 4 ? 2 : 1;
+#pragma unroll
+        for (int r = 0; r < QREQ; ++r)
+          tma_load_5d(sQ + r * (C::QCH / QREQ) * kChunkB, &tm_q, 0, w.q0, r * (C::QCH / QREQ), w.h, w.b, qb);
+        ++nq;
+        auto load_k = [&](int kt) {
+          for (int p2 = 0; p2 < C::KPARTS && ok; ++p2) {
+            if (!thread_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, a.err, abort)) { ok = false; break; }
+            const uint32_t fb = smem_u32(&bars->full[slot]);
+            mbar_arrive_expect_tx(fb, C::KPB);
+            tma_load_5d(sRing + slot * C::SLOTB, &tm_k, 0, kt * kBN, p2 * C::CPP, w.kvh, w.b, fb);
+            advance();
+          }
+        };
+        auto load_v = [&](int kt) {
+          for (int p2 = 0; p2 < C::VPARTS && ok; ++p2) {
+            if (!thread_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, a.err, abort)) { ok = false; break; }
+            const uint32_t fb = smem_u32(&bars->full[slot]);
+            mbar_arrive_expect_tx(fb, C::VPB);
+            tma_load_5d(sRing + slot * C::SLOTB, &tm_v, 0, kt * kBN + p2 * C::VKP, w.dh * (C::DV / 64), w.kvh, w.b,
+                        fb);
+            advance();
+          }
+        };
+        load_k(w.kt_begin);
+        for (int j = 0; j < w.ntiles && ok; ++j) {
+          if (j + 1 < w.ntiles) load_k(w.kt_begin + j + 1);
+          load_v(w.kt_begin + j);
         }
-      };
-      auto load_v = [&](int kt) {
-        for (int p2 = 0; p2 < C::VPARTS && ok; ++p2) {
-          if (!thread_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, a.err, abort)) { ok = false; break; }
-          const uint32_t fb = smem_u32(&bars->full[slot]);
-          mbar_arrive_expect_tx(fb, C::VPB);
-          tma_load_5d(sRing + slot * C::SLOTB, &tm_v, 0, kt * kBN + p2 * C::VKP, dh * (C::DV / 64), kvh, b, fb);
-          advance();
-        }
-      };
-      load_k(kt_begin);
-      for (int j = 0; j < ntiles && ok; ++j) {
-        if (j + 1 < ntiles) load_k(kt_begin + j + 1);
-        load_v(kt_begin + j);
       }
       // Copies still in flight must land before the CTA may exit.
-      thread_wait(smem_u32(&bars->q_full), 0, nullptr);
+      if (nq > 0) thread_wait(qb, (nq - 1) & 1, nullptr);
       for (int s2 = max(0, seq - C::NSLOT); s2 < seq; ++s2)
         thread_wait(smem_u32(&bars->full[s2 % C::NSLOT]), (s2 / C::NSLOT) & 1, nullptr);
     }
@@ -240,12 +293,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // One lane waits and issues (tcgen05.mma is issued by a single thread;
-    // waiting with the whole warp only adds latency between MMAs).
-    if (lane == 0 && ntiles > 0) {
+    // waiting with the whole warp only adds latency between MMAs).  Tile
+    // parities run on across items (J counts every tile of the CTA).
+    if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, C::DV, 0, 1);
-      bool ok = thread_wait(smem_u32(&bars->q_full), 0, a.err, abort);
-      tc_fence_after();
+      bool ok = true;
       // Descriptors are built once; a slot, a 64-dim chunk or a 16-element
       // K step only moves the start address (16-byte units in the low bits,
       // which stay below 2^14 for any shared-memory address).  Building them
@@ -261,8 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t soff = 0;   // slot * SLOTB in descriptor units (16 bytes)
       const uint32_t full0 = smem_u32(&bars->full[0]);
       const uint32_t empty0 = smem_u32(&bars->empty[0]);
-      auto release = [&]() {
-        tc_commit(empty0 + slot * 8);
+      auto advance = [&]() {
         soff += C::SLOTB >> 4;
         if (++slot == C::NSLOT) {
           slot = 0;
@@ -270,68 +322,90 @@ __global__ void __launch_bounds__(kThreads, 1)
           soff = 0;
         }
       };
-      auto mma_qk = [&](int j) {
-        const int sb = j & 1;
-        const uint32_t dS = tmem + sb * kBN;
-        uint64_t ad = dq0;
-#pragma unroll 1
-        for (int p2 = 0; p2 < C::KPARTS; ++p2) {
-          if (!thread_wait(full0 + slot * 8, phase, a.err, abort)) { ok = false; return; }
-          tc_fence_after();
-          uint64_t bd = dk0 + soff;
-#pragma unroll
-          for (int c = 0; c < C::CPP; ++c) {
-            tc_mma_ss(dS, ad, bd, idesc_qk, (p2 > 0 || c > 0) ? 1u : 0u);
-            tc_mma_ss(dS, ad + 2, bd + 2, idesc_qk, 1u);
-            tc_mma_ss(dS, ad + 4, bd + 4, idesc_qk, 1u);
-            tc_mma_ss(dS, ad + 6, bd + 6, idesc_qk, 1u);
-            ad += kChunkB >> 4;
-            bd += kChunkB >> 4;
-          }
-          release();
-        }
-        tc_commit(smem_u32(&bars->s_full[sb]));
+      auto release = [&]() {
+        tc_commit(empty0 + slot * 8);
+        advance();
       };
-      auto mma_pv = [&](int j) {
-        const int sb = j & 1;
-        if (!thread_wait(smem_u32(&bars->p_full[sb]), (j >> 1) & 1, a.err, abort)) { ok = false; return; }
+      int J = 0;   // tiles of earlier items
+      int nq = 0;  // items started
+      for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+        const TcItem w = tc_item<C::NDH>(a, it, nqt);
+        if (w.ntiles == 0) continue;
+        if (!thread_wait(smem_u32(&bars->q_full), nq & 1, a.err, abort)) break;
+        ++nq;
         tc_fence_after();
-        const int kt = kt_begin + j;
-        uint32_t ta = tmem + sb * kBN;  // P_j: 128 keys as 64 packed columns
+        auto mma_qk = [&](int j) {
+          const int sb = (J + j) & 1;
+          const uint32_t dS = tmem + sb * kBN;
+          uint64_t ad = dq0;
 #pragma unroll 1
-        for (int p2 = 0; p2 < C::VPARTS; ++p2) {
-          if (!thread_wait(full0 + slot * 8, phase, a.err, abort)) { ok = false; return; }
-          // Rows of keys past the cache's filled length may hold anything
-          // (even NaN, and 0 * NaN = NaN); zero them before they meet P
-          // (only in the part holding the end of the keys).
-          const int key0 = kt * kBN + p2 * C::VKP;
-          if (key0 + C::VKP > Lk) {
-            const int nvalid = max(0, Lk - key0);
-            uint8_t* slot_ptr = smem + C::RING_OFF + slot * C::SLOTB;
-            const int nbad = C::VKP - nvalid;
-            for (int i = 0; i < (C::DV / 64) * nbad * 8; ++i) {
-              const int dc = i / (nbad * 8);
-              const int rr = (i / 8) % nbad + nvalid;
-              const int pc = i % 8;
-              *reinterpret_cast<uint4*>(slot_ptr + dc * C::VKP * 128 + rr * 128 + pc * 16) = make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-          }
-          tc_fence_after();
-          const uint64_t bd = dv0 + soff;
+          for (int p2 = 0; p2 < C::KPARTS; ++p2) {
+            if (!thread_wait(full0 + slot * 8, phase, a.err, abort)) { ok = false; return; }
+            tc_fence_after();
+            uint64_t bd = dk0 + soff;
 #pragma unroll
-          for (int kk = 0; kk < C::VKP / 16; ++kk)
-            tc_mma_ts(tmem_O, ta + kk * 8, bd + static_cast<uint64_t>(kk * 128), idesc_pv,
-                      (j > 0 || p2 > 0 || kk > 0) ? 1u : 0u);
-          ta += C::VKP / 2;
-          release();
+            for (int c = 0; c < C::CPP; ++c) {
+              tc_mma_ss(dS, ad, bd, idesc_qk, (p2 > 0 || c > 0) ? 1u : 0u);
+              tc_mma_ss(dS, ad + 2, bd + 2, idesc_qk, 1u);
+              tc_mma_ss(dS, ad + 4, bd + 4, idesc_qk, 1u);
+              tc_mma_ss(dS, ad + 6, bd + 6, idesc_qk, 1u);
+              ad += kChunkB >> 4;
+              bd += kChunkB >> 4;
+            }
+            release();
+          }
+          tc_commit(smem_u32(&bars->s_full[sb]));
+          // after the item's last QK, the Q area may take the next item's Q
+          if (j == w.ntiles - 1) tc_commit(smem_u32(&bars->q_free));
+        };
+        auto mma_pv = [&](int j) {
+          const int sb = (J + j) & 1;
+          if (!thread_wait(smem_u32(&bars->p_full[sb]), ((J + j) >> 1) & 1, a.err, abort)) { ok = false; return; }
+          tc_fence_after();
+          const int kt = w.kt_begin + j;
+          uint32_t ta = tmem + sb * kBN;  // P_j: 128 keys as 64 packed columns
+          const bool last = j == w.ntiles - 1;
+#pragma unroll 1
+          for (int p2 = 0; p2 < C::VPARTS; ++p2) {
+            if (!thread_wait(full0 + slot * 8, phase, a.err, abort)) { ok = false; return; }
+            // Rows of keys past the cache's filled length may hold anything
+            // (even NaN, and 0 * NaN = NaN); zero them before they meet P
+            // (only in the part holding the end of the keys).
+            const int key0 = kt * kBN + p2 * C::VKP;
+            if (key0 + C::VKP > w.Lk) {
+              const int nvalid = max(0, w.Lk - key0);
+              uint8_t* slot_ptr = smem + C::RING_OFF + slot * C::SLOTB;
+              const int nbad = C::VKP - nvalid;
+              for (int i = 0; i < (C::DV / 64) * nbad * 8; ++i) {
+                const int dc = i / (nbad * 8);
+                const int rr = (i / 8) % nbad + nvalid;
+                const int pc = i % 8;
+                *reinterpret_cast<uint4*>(slot_ptr + dc * C::VKP * 128 + rr * 128 + pc * 16) = make_uint4(0, 0, 0, 0);
+              }
+              fence_proxy_async_smem();
+            }
+            tc_fence_after();
+            const uint64_t bd = dv0 + soff;
+#pragma unroll
+            for (int kk = 0; kk < C::VKP / 16; ++kk)
+              tc_mma_ts(tmem_O, ta + kk * 8, bd + static_cast<uint64_t>(kk * 128), idesc_pv,
+                        (j > 0 || p2 > 0 || kk > 0) ? 1u : 0u);
+            ta += C::VKP / 2;
+            // The item's last OSLOTS V parts stay held: the epilogue stages
+            // O there and frees them after its store has read them.
+            if (last && p2 >= C::VPARTS - C::OSLOTS)
+              advance();
+            else
+              release();
+          }
+          tc_commit(smem_u32(&bars->o_done[sb]));
+        };
+        mma_qk(0);
+        for (int j = 0; j < w.ntiles && ok; ++j) {
+          if (j + 1 < w.ntiles) mma_qk(j + 1);
+          if (ok) mma_pv(j);
         }
-        tc_commit(smem_u32(&bars->o_done[sb]));
-      };
-      if (ok) mma_qk(0);
-      for (int j = 0; j < ntiles && ok; ++j) {
-        if (j + 1 < ntiles) mma_qk(j + 1);
-        if (ok) mma_pv(j);
+        J += w.ntiles;
       }
       // Every MMA issued so far completes before TMEM is released.
       tc_commit(smem_u32(&bars->drain));
@@ -344,169 +418,203 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = (warp - 2) >> 2;  // which 64 of the 128 score columns
     const int r = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const int qpos = qpos_first + r;
-    const bool row_valid = r < valid_rows;
     const float c2 = a.scale_log2;  // > 0 (checked on the host)
     constexpr int kHB = kBN / 2;    // score columns per thread
     constexpr int kDVH = C::DV / 2; // O columns per thread
-    float m = -INFINITY;  // exponent base in log2 units: a stale running maximum
-    float l = 0.0f;       // this half's share of the row sum
-    bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
-      const int sb = j & 1;
-      if (!warp_wait(smem_u32(&bars->s_full[sb]), (j >> 1) & 1, a.err, abort)) { ok = false; break; }
-      tc_fence_after();
-      float s[kHB];
-      float mt;
-      {
-        // the whole row: both threads of a row take the same maximum
-        uint32_t r0[32], r1[32], o0[32], o1[32];
-        const uint32_t tS = tmem + lane_off + sb * kBN;
-        tmem_ld32(tS + half * kHB, r0);
-        tmem_ld32(tS + half * kHB + 32, r1);
-        tmem_ld32(tS + (1 - half) * kHB, o0);
-        tmem_ld32(tS + (1 - half) * kHB + 32, o1);
-        tc_wait_ld();
+    constexpr int kParts = C::KPARTS + C::VPARTS;  // ring parts per key tile
+    int J = 0;      // tiles of earlier items
+    int nq = 0;     // items done
+    int parts = 0;  // ring parts of earlier items
+    for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+      const TcItem w = tc_item<C::NDH>(a, it, nqt);
+      const int ntiles = w.ntiles;
+      if (ntiles == 0) {
+        // No visible key (only reachable with out-of-contract positions).
+        if (r < w.valid_rows) {
+          __nv_bfloat16* dst =
+              static_cast<__nv_bfloat16*>(a.out) +
+              (((static_cast<size_t>(w.b) * a.T + w.q0 + r) * a.H + w.h) * HD + w.dh * C::DV + half * kDVH);
+          for (int i = 0; i < kDVH / 8; ++i) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
+        }
+        continue;
+      }
+      const int qpos = w.qpos_first + r;
+      const bool row_valid = r < w.valid_rows;
+      float m = -INFINITY;  // exponent base in log2 units: a stale running maximum
+      float l = 0.0f;       // this half's share of the row sum
+      bool ok = true;
+      for (int j = 0; j < ntiles; ++j) {
+        const int sb = (J + j) & 1;
+        if (!warp_wait(smem_u32(&bars->s_full[sb]), ((J + j) >> 1) & 1, a.err, abort)) { ok = false; break; }
+        tc_fence_after();
+        float s[kHB];
+        float mt;
+        {
+          // the whole row: both threads of a row take the same maximum
+          uint32_t r0[32], r1[32], o0[32], o1[32];
+          const uint32_t tS = tmem + lane_off + sb * kBN;
+          tmem_ld32(tS + half * kHB, r0);
+          tmem_ld32(tS + half * kHB + 32, r1);
+          tmem_ld32(tS + (1 - half) * kHB, o0);
+          tmem_ld32(tS + (1 - half) * kHB + 32, o1);
+          tc_wait_ld();
+          // P_j goes over S_j, partly over the other warp's half of the row,
+          // which that warp reads too: tell it this warp's reads are done.
+          mbar_arrive(smem_u32(&bars->s_read[quarter]));
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            s[i] = __uint_as_float(r0[i]);
+            s[32 + i] = __uint_as_float(r1[i]);
+          }
+          const int kr = (w.kt_begin + j) * kBN;
+          const bool row_vis = row_valid && (kr + kBN - 1 <= qpos) && (kr + kBN <= w.Lk) &&
+                               (!a.sliding || qpos - kr < a.window);
+          const int k0 = kr + half * kHB;
+          const int k1 = kr + (1 - half) * kHB;
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (row_vis) {
+#pragma unroll
+            for (int n = 0; n < 32; ++n) {
+              mx[n & 3] = fmaxf(mx[n & 3], fmaxf(s[n], s[32 + n]));
+              mx[(n + 2) & 3] = fmaxf(mx[(n + 2) & 3], fmaxf(__uint_as_float(o0[n]), __uint_as_float(o1[n])));
+            }
+          } else {
+            // The row's visible keys are one interval [vlo, vhi): causal end,
+            // the cache's filled length and (sliding) the window start.
+            const int vlo = a.sliding ? max(0, qpos - a.window + 1) : 0;
+            const int vhi = row_valid ? min(qpos + 1, w.Lk) : 0;
+            const unsigned span = static_cast<unsigned>(max(0, vhi - vlo));
+            const int lo0 = vlo - k0, lo1 = vlo - k1;
+#pragma unroll
+            for (int n = 0; n < kHB; ++n) {
+              if (static_cast<unsigned>(n - lo0) >= span) s[n] = -INFINITY;
+              mx[n & 3] = fmaxf(mx[n & 3], s[n]);
+            }
+#pragma unroll
+            for (int n = 0; n < 32; ++n) {
+              const float v0 = static_cast<unsigned>(n - lo1) < span ? __uint_as_float(o0[n]) : -INFINITY;
+              const float v1 = static_cast<unsigned>(n + 32 - lo1) < span ? __uint_as_float(o1[n]) : -INFINITY;
+              mx[n & 3] = fmaxf(mx[n & 3], fmaxf(v0, v1));
+            }
+          }
+          mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
+        }
+        float alpha = 1.0f;
+        bool rescale = false;
+        float m_use = m;
+        if (m == -INFINITY) {
+          m_use = mt;  // nothing accumulated yet (O row is zero or unwritten)
+        } else if (mt - m > kRescaleLog2) {
+          m_use = mt;
+          alpha = ex2_approx(m - mt);
+          rescale = true;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+          // A row of this warp raises its base (only after a tile with a
+          // visible key, so j > 0): PV_{j-1} must be complete before the O
+          // rows are scaled; PV_j is not issued until P_j below is published.
+          if (!warp_wait(smem_u32(&bars->o_done[(J + j - 1) & 1]), ((J + j - 1) >> 1) & 1, a.err, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float f = rescale ? alpha : 1.0f;
+#pragma unroll 1
+          for (int cc = 0; cc < kDVH / 32; ++cc) {
+            uint32_t rr[32];
+            const uint32_t tO = tmem_O + lane_off + half * kDVH + cc * 32;
+            tmem_ld32(tO, rr);
+            tc_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * f);
+            tmem_st32(tO, rr);
+          }
+          tc_wait_st();
+        }
+        const float nb = (m_use == -INFINITY) ? 0.0f : -m_use;
+        uint32_t p[32];
+        float sa[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          s[i] = __uint_as_float(r0[i]);
-          s[32 + i] = __uint_as_float(r1[i]);
+          const uint32_t pw = pack_bf16x2(ex2_approx(fmaf(s[2 * i], c2, nb)), ex2_approx(fmaf(s[2 * i + 1], c2, nb)));
+          p[i] = pw;
+          sa[(2 * i) & 3] += bf16_lo(pw);
+          sa[(2 * i + 1) & 3] += bf16_hi(pw);
         }
-        const int kr = (kt_begin + j) * kBN;
-        const bool row_vis = row_valid && (kr + kBN - 1 <= qpos) && (kr + kBN <= Lk) &&
-                             (!a.sliding || qpos - kr < a.window);
-        const int k0 = kr + half * kHB;
-        const int k1 = kr + (1 - half) * kHB;
-        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-        if (row_vis) {
-#pragma unroll
-          for (int n = 0; n < 32; ++n) {
-            mx[n & 3] = fmaxf(mx[n & 3], fmaxf(s[n], s[32 + n]));
-            mx[(n + 2) & 3] = fmaxf(mx[(n + 2) & 3], fmaxf(__uint_as_float(o0[n]), __uint_as_float(o1[n])));
-          }
-        } else {
-          // The row's visible keys are one interval [vlo, vhi): causal end,
-          // the cache's filled length and (sliding) the window start.
-          const int vlo = a.sliding ? max(0, qpos - a.window + 1) : 0;
-          const int vhi = row_valid ? min(qpos + 1, Lk) : 0;
-          const unsigned span = static_cast<unsigned>(max(0, vhi - vlo));
-          const int lo0 = vlo - k0, lo1 = vlo - k1;
-#pragma unroll
-          for (int n = 0; n < kHB; ++n) {
-            if (static_cast<unsigned>(n - lo0) >= span) s[n] = -INFINITY;
-            mx[n & 3] = fmaxf(mx[n & 3], s[n]);
-          }
-#pragma unroll
-          for (int n = 0; n < 32; ++n) {
-            const float v0 = static_cast<unsigned>(n - lo1) < span ? __uint_as_float(o0[n]) : -INFINITY;
-            const float v1 = static_cast<unsigned>(n + 32 - lo1) < span ? __uint_as_float(o1[n]) : -INFINITY;
-            mx[n & 3] = fmaxf(mx[n & 3], fmaxf(v0, v1));
-          }
-        }
-        mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
-      }
-      float alpha = 1.0f;
-      bool rescale = false;
-      float m_use = m;
-      if (m == -INFINITY) {
-        m_use = mt;  // nothing accumulated yet (O row is zero or unwritten)
-      } else if (mt - m > kRescaleLog2) {
-        m_use = mt;
-        alpha = ex2_approx(m - mt);
-        rescale = true;
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-        // A row of this warp raises its base (only after a tile with a
-        // visible key, so j > 0): PV_{j-1} must be complete before the O
-        // rows are scaled; PV_j is not issued until P_j below is published.
-        if (!warp_wait(smem_u32(&bars->o_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, a.err, abort)) {
+        if (!warp_wait(smem_u32(&bars->s_read[quarter]), (J + j) & 1, a.err, abort)) {
           ok = false;
           break;
         }
-        tc_fence_after();
-        const float f = rescale ? alpha : 1.0f;
-#pragma unroll 1
-        for (int cc = 0; cc < kDVH / 32; ++cc) {
-          uint32_t rr[32];
-          const uint32_t tO = tmem_O + lane_off + half * kDVH + cc * 32;
-          tmem_ld32(tO, rr);
+        tmem_st32(tmem + lane_off + sb * kBN + half * (kHB / 2), p);
+        l = l * alpha + ((sa[0] + sa[1]) + (sa[2] + sa[3]));
+        m = m_use;
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->p_full[sb]));
+      }
+      if (ok) {
+        // the full row sum: both halves' shares
+        bars->red[half][r] = l;
+        mbar_arrive(smem_u32(&bars->sum_full[quarter]));
+        ok = warp_wait(smem_u32(&bars->sum_full[quarter]), nq & 1, a.err, abort);
+        l = bars->red[0][r] + bars->red[1][r];
+      }
+      // Epilogue: O / l as bf16, in the chunk-major 128-byte-swizzled layout of
+      // the output tensor map, into the ring slots of the item's last V parts
+      // (free once the last PV has completed), then TMA stores of the tile.
+      // Rows past T fall outside the map and are not written.
+      const int last_part = parts + ntiles * kParts - 1;  // ring sequence number
+      auto oslot = [&](int k) { return (last_part - (C::OSLOTS - 1) + k) % C::NSLOT; };
+      if (ok) {
+        const int jl = J + ntiles - 1;
+        if (warp_wait(smem_u32(&bars->o_done[jl & 1]), (jl >> 1) & 1, a.err, abort)) {
+          tc_fence_after();
+          const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
+          constexpr int NCC = kDVH / 32;
+          uint32_t rr[NCC][32];
+#pragma unroll
+          for (int cc = 0; cc < NCC; ++cc) tmem_ld32(tmem_O + lane_off + half * kDVH + cc * 32, rr[cc]);
           tc_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) rr[i] = __float_as_uint(__uint_as_float(rr[i]) * f);
-          tmem_st32(tO, rr);
-        }
-        tc_wait_st();
-      }
-      const float nb = (m_use == -INFINITY) ? 0.0f : -m_use;
-      uint32_t p[32];
-      float sa[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          for (int cc = 0; cc < NCC; ++cc) {
+            // 32 columns = half a 64-column chunk: pieces (16 bytes) p0 .. p0 + 3
+            const int col = half * kDVH + cc * 32;
+            const int ch = col / 64;
+            const uint32_t row_addr = sRing + oslot(ch / C::CPS) * C::SLOTB + (ch % C::CPS) * kChunkB + r * 128;
+            const int p0 = (col % 64) / 8;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const uint32_t w = pack_bf16x2(ex2_approx(fmaf(s[2 * i], c2, nb)), ex2_approx(fmaf(s[2 * i + 1], c2, nb)));
-        p[i] = w;
-        sa[(2 * i) & 3] += bf16_lo(w);
-        sa[(2 * i + 1) & 3] += bf16_hi(w);
-      }
-      tmem_st32(tmem + lane_off + sb * kBN + half * (kHB / 2), p);
-      l = l * alpha + ((sa[0] + sa[1]) + (sa[2] + sa[3]));
-      m = m_use;
-      tc_wait_st();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars->p_full[sb]));
-    }
-    if (ntiles > 0 && ok) {
-      // the full row sum: both halves' shares
-      bars->red[half][r] = l;
-      mbar_arrive(smem_u32(&bars->sum_full[quarter]));
-      ok = warp_wait(smem_u32(&bars->sum_full[quarter]), 0, a.err, abort);
-      l = bars->red[0][r] + bars->red[1][r];
-    }
-    // Epilogue: O / l as bf16 into shared memory (the Q area: every MMA has
-    // completed once the last PV has), in the chunk-major 128-byte-swizzled
-    // layout of the output tensor map, then one TMA store of the tile.  Rows
-    // past T fall outside the map and are not written.
-    if (ntiles > 0 && ok) {
-      const int jl = ntiles - 1;
-      if (warp_wait(smem_u32(&bars->o_done[jl & 1]), (jl >> 1) & 1, a.err, abort)) {
-        tc_fence_after();
-        const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
-        constexpr int NCC = kDVH / 32;
-        uint32_t rr[NCC][32];
-#pragma unroll
-        for (int cc = 0; cc < NCC; ++cc) tmem_ld32(tmem_O + lane_off + half * kDVH + cc * 32, rr[cc]);
-        tc_wait_ld();
-#pragma unroll
-        for (int cc = 0; cc < NCC; ++cc) {
-          // 32 columns = half a 64-column chunk: pieces (16 bytes) p0 .. p0 + 3
-          const int col = half * kDVH + cc * 32;
-          const uint32_t row_addr = sQ + (col / 64) * kChunkB + r * 128;
-          const int p0 = (col % 64) / 8;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t x = pack_bf16x2(__uint_as_float(rr[cc][8 * i + 0]) * inv_l, __uint_as_float(rr[cc][8 * i + 1]) * inv_l);
-            const uint32_t y = pack_bf16x2(__uint_as_float(rr[cc][8 * i + 2]) * inv_l, __uint_as_float(rr[cc][8 * i + 3]) * inv_l);
-            const uint32_t z = pack_bf16x2(__uint_as_float(rr[cc][8 * i + 4]) * inv_l, __uint_as_float(rr[cc][8 * i + 5]) * inv_l);
-            const uint32_t w = pack_bf16x2(__uint_as_float(rr[cc][8 * i + 6]) * inv_l, __uint_as_float(rr[cc][8 * i + 7]) * inv_l);
-            const uint32_t addr = row_addr + (((p0 + i) ^ (r & 7)) * 16);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(w)
-                         : "memory");
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t x = pack_bf16x2(__uint_as_float(rr[cc][8 * i + 0]) * inv_l, __uint_as_float(rr[cc][8 * i + 1]) * inv_l);
+              const uint32_t y = pack_bf16x2(__uint_as_float(rr[cc][8 * i + 2]) * inv_l, __uint_as_float(rr[cc][8 * i + 3]) * inv_l);
+              const uint32_t z = pack_bf16x2(__uint_as_float(rr[cc][8 * i + 4]) * inv_l, __uint_as_float(rr[cc][8 * i + 5]) * inv_l);
+              const uint32_t q = pack_bf16x2(__uint_as_float(rr[cc][8 * i + 6]) * inv_l, __uint_as_float(rr[cc][8 * i + 7]) * inv_l);
+              const uint32_t addr = row_addr + (((p0 + i) ^ (r & 7)) * 16);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(x), "r"(y), "r"(z), "r"(q)
+                           : "memory");
+            }
           }
+          fence_proxy_async_smem();
+        } else {
+          ok = false;
         }
-        fence_proxy_async_smem();
       }
-    } else if (ntiles == 0 && r < valid_rows) {
-      // No visible key (only reachable with out-of-contract positions).
-      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
-                           (((static_cast<size_t>(b) * a.T + q0 + r) * a.H + h) * HD + dh * C::DV + half * kDVH);
-      for (int i = 0; i < kDVH / 8; ++i) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
-    }
-    // All 256 softmax threads meet here on every path (named barrier 1);
-    // after an abort the tile is left unwritten.
-    asm volatile("bar.sync 1, 256;" ::: "memory");
-    if (warp == 2 && lane == 0 && ntiles > 0 && !*abort) {
-      tma_store_5d(&tm_o, sQ, 0, q0, dh * (C::DV / 64), h, b);
-      bulk_commit_group();
-      bulk_wait_read_all();  // the tile's shared memory must outlive the copy's reads
+      // All 256 softmax threads meet here on every path, and all leave the
+      // item loop together if any wait anywhere gave up.
+      const bool stop = softmax_sync_any(!ok || *abort);
+      if (warp == 2 && lane == 0 && !stop) {
+#pragma unroll
+        for (int k = 0; k < C::OSLOTS; ++k)
+          tma_store_5d(&tm_o, sRing + oslot(k) * C::SLOTB, 0, w.q0, w.dh * (C::DV / 64) + k * C::CPS, w.h, w.b);
+        bulk_commit_group();
+        bulk_wait_read_all();  // the slots must not be refilled before the stores have read them
+#pragma unroll
+        for (int k = 0; k < C::OSLOTS; ++k) mbar_arrive(smem_u32(&bars->empty[oslot(k)]));
+      }
+      __syncwarp();
+      if (stop) break;
+      J += ntiles;
+      parts += ntiles * kParts;
+      ++nq;
     }
   }
 
@@ -587,11 +695,15 @@ cudaError_t launch_hd(const PrefillTcArgs& a, cudaStream_t s) {
     const cuuint64_t dims[5] = {64, static_cast<cuuint64_t>(a.T), static_cast<cuuint64_t>(C::QCH),
                                 static_cast<cuuint64_t>(a.H), static_cast<cuuint64_t>(a.B)};
     const cuuint64_t str[4] = {row_b * a.H, 128, row_b, row_b * a.H * a.T};
-    const cuuint32_t box[5] = {64, kBM, C::DV / 64, 1, 1};
+    const cuuint32_t box[5] = {64, kBM, C::CPS, 1, 1};
     if (!make_map(&mo, a.out, dims, str, box)) return cudaErrorInvalidValue;
   }
+  // One persistent CTA per SM (shared memory and TMEM allow no more), each
+  // taking work items blockIdx.x, blockIdx.x + gridDim.x, ...
   const int nqt = (a.T + kBM - 1) / kBM;
-  const long long nblk = static_cast<long long>(nqt) * a.H * a.B * C::NDH;
+  const long long nitems = static_cast<long long>(nqt) * a.H * a.B * C::NDH;
+  if (nitems > 0x7fffffffLL) return cudaErrorInvalidValue;
+  const long long nblk = nitems < sm_count() ? nitems : sm_count();
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(nblk));
   cfg.blockDim = dim3(kThreads);
