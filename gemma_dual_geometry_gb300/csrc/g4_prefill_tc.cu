@@ -38,7 +38,9 @@
 //               only when it grows by more than 2^64 (the stale maximum is
 //               exact for O / l), rescale its half of the O row in TMEM when
 //               it is raised, and write its P half as bf16 over the S buffer
-//               (packed: 32 columns).  The row sum l adds the bf16-rounded P
+//               (packed: 32 columns), once the other warp of the quarter has
+//               read the row too (P lands on S columns both warps read).
+//               The row sum l adds the bf16-rounded P
 //               values, the weights the PV MMA really applies, so a row
 //               dominated by one key returns that key's value without the
 //               rounding error of P; the two halves' sums meet in shared
