@@ -81,6 +81,7 @@ struct PrefillTcArgs {
   int B, T, H, Hkv, hd, max_len;
   int sliding, window;
   float scale_log2;
+  unsigned* item_ctr;  // [2]: next work item, CTAs done (zero between launches; set by the launcher)
 };
 cudaError_t launch_prefill_tc(const PrefillTcArgs& a, cudaStream_t s);
 

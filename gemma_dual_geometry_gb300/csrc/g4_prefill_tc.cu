@@ -11,8 +11,9 @@
 // then recompute the same scores; TMEM holds 512 f32 columns per SM and a
 // 128 x 512 accumulator alone would fill it).  Items run in (sequence, kv
 // head) groups, heaviest query tiles first, so the CTAs in flight share their
-// K / V in L2.  The kernel is persistent: one CTA per SM takes items
-// blockIdx.x, blockIdx.x + gridDim.x, ..., with its barriers, ring and TMEM
+// K / V in L2.  The kernel is persistent: one CTA per SM takes items one
+// after another from a global counter (the producer draws them and passes
+// them on through a 4-entry queue in shared memory), with its barriers, ring and TMEM
 // running on from item to item, so the next item's Q and first K parts load
 // while the current one finishes.  Warp roles (320 threads):
 //   warp 0      TMA producer (one lane): the Q tile, then K parts (128 keys x
@@ -54,6 +55,8 @@
 // keeps each phase unambiguous for waiters that skip phases.
 // Key tiles wholly outside every row's band are never loaded.
 #include <math.h>
+
+#include <mutex>
 
 #include "g4_device.cuh"
 #include "g4_internal.h"
@@ -117,6 +120,9 @@ struct TcBars {
   uint64_t s_read[4];    // [lane quarter]: both warps have S_j in registers (P_j may overwrite it)
   uint64_t full[kMaxSlots];
   uint64_t empty[kMaxSlots];
+  uint64_t it_full[4];   // work-item queue entry written (by the producer)
+  uint64_t it_empty[4];  // entry read by the MMA issuer and the softmax warps
+  int items[4];          // work-item queue: item index, or -1 when none is left
   uint32_t tmem_base;
   int abort;
   float red[2][kBM];  // [column half][row]: row-sum shares
@@ -213,6 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int qq = 0; qq < 4; ++qq) mbar_init(smem_u32(&bars->s_read[qq]), 64);
     for (int i = 0; i < C::NSLOT; ++i) mbar_init(smem_u32(&bars->full[i]), 1);
     for (int i = 0; i < C::NSLOT; ++i) mbar_init(smem_u32(&bars->empty[i]), 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(smem_u32(&bars->it_full[i]), 1);
+      mbar_init(smem_u32(&bars->it_empty[i]), 2);
+    }
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -250,7 +260,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           phase ^= 1u;
         }
       };
-      for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+      for (int n = 0; ok; ++n) {
+        // next work item into queue entry n % 4 (once both readers are done with its last use)
+        const int e = n & 3;
+        if (n >= 4 && !thread_wait(smem_u32(&bars->it_empty[e]), ((n >> 2) - 1) & 1, a.err, abort)) break;
+        const unsigned got = atomicAdd(a.item_ctr, 1u);
+        const int it = got < static_cast<unsigned>(nitems) ? static_cast<int>(got) : -1;
+        *reinterpret_cast<volatile int*>(&bars->items[e]) = it;
+        mbar_arrive(smem_u32(&bars->it_full[e]));
+        if (it < 0) break;
         const TcItem w = tc_item<C::NDH>(a, it, nqt);
         if (w.ntiles == 0) continue;
         if (nq > 0 && !thread_wait(smem_u32(&bars->q_free), (nq - 1) & 1, a.err, abort)) break;
@@ -330,7 +348,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       int J = 0;   // tiles of earlier items
       int nq = 0;  // items started
-      for (int it = blockIdx.x; it < nitems && ok; it += gridDim.x) {
+      for (int n = 0; ok; ++n) {
+        const int e = n & 3;
+        if (!thread_wait(smem_u32(&bars->it_full[e]), (n >> 2) & 1, a.err, abort)) break;
+        const int it = *reinterpret_cast<volatile int*>(&bars->items[e]);
+        mbar_arrive(smem_u32(&bars->it_empty[e]));
+        if (it < 0) break;
         const TcItem w = tc_item<C::NDH>(a, it, nqt);
         if (w.ntiles == 0) continue;
         if (!thread_wait(smem_u32(&bars->q_full), nq & 1, a.err, abort)) break;
@@ -427,7 +450,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     int J = 0;      // tiles of earlier items
     int nq = 0;     // items done
     int parts = 0;  // ring parts of earlier items
-    for (int it = blockIdx.x; it < nitems; it += gridDim.x) {
+    for (int n = 0;; ++n) {
+      const int e = n & 3;
+      const int it = warp_wait(smem_u32(&bars->it_full[e]), (n >> 2) & 1, a.err, abort)
+                         ? *reinterpret_cast<volatile int*>(&bars->items[e])
+                         : -1;
+      if (it < 0) {
+        // no item left (or a wait gave up): every softmax thread leaves here
+        // or at the end of an item, together
+        softmax_sync_any(1);
+        break;
+      }
       const TcItem w = tc_item<C::NDH>(a, it, nqt);
       const int ntiles = w.ntiles;
       if (ntiles == 0) {
@@ -438,6 +471,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               (((static_cast<size_t>(w.b) * a.T + w.q0 + r) * a.H + w.h) * HD + w.dh * C::DV + half * kDVH);
           for (int i = 0; i < kDVH / 8; ++i) reinterpret_cast<uint4*>(dst)[i] = make_uint4(0, 0, 0, 0);
         }
+        const bool stop0 = softmax_sync_any(*abort);
+        if (warp == 2 && lane == 0 && !stop0) mbar_arrive(smem_u32(&bars->it_empty[e]));
+        __syncwarp();
+        if (stop0) break;
         continue;
       }
       const int qpos = w.qpos_first + r;
@@ -612,6 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < C::OSLOTS; ++k) mbar_arrive(smem_u32(&bars->empty[oslot(k)]));
       }
+      if (warp == 2 && lane == 0 && !stop) mbar_arrive(smem_u32(&bars->it_empty[e]));
       __syncwarp();
       if (stop) break;
       J += ntiles;
@@ -625,6 +663,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
+  }
+  // The last CTA to finish (every CTA has drawn its last item by now) clears
+  // the counters for the next launch that uses them.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.item_ctr + 1, 1u) == gridDim.x - 1) {
+      __threadfence();
+      atomicExch(a.item_ctr, 0u);
+      atomicExch(a.item_ctr + 1, 0u);
+    }
   }
 }
 
@@ -701,7 +749,7 @@ cudaError_t launch_hd(const PrefillTcArgs& a, cudaStream_t s) {
     if (!make_map(&mo, a.out, dims, str, box)) return cudaErrorInvalidValue;
   }
   // One persistent CTA per SM (shared memory and TMEM allow no more), each
-  // taking work items blockIdx.x, blockIdx.x + gridDim.x, ...
+  // drawing work items from the launch's counter pair until none is left.
   const int nqt = (a.T + kBM - 1) / kBM;
   const long long nitems = static_cast<long long>(nqt) * a.H * a.B * C::NDH;
   if (nitems > 0x7fffffffLL) return cudaErrorInvalidValue;
@@ -721,7 +769,30 @@ cudaError_t launch_hd(const PrefillTcArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_prefill_tc(const PrefillTcArgs& a, cudaStream_t s) {
+// Work-item counters of the persistent prefill, one pair per launch in flight
+// (launches take the pairs in turn, so up to kCtrSlots launches may overlap).
+constexpr int kCtrSlots = 64;
+__device__ unsigned g_prefill_ctr[kCtrSlots][2];
+
+cudaError_t launch_prefill_tc(const PrefillTcArgs& a_in, cudaStream_t s) {
+  static std::mutex mu;
+  static unsigned* base[128] = {};
+  static unsigned next_slot = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  PrefillTcArgs a = a_in;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (base[dev] == nullptr) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_prefill_ctr);
+      if (e != cudaSuccess) return e;
+      base[dev] = static_cast<unsigned*>(p);
+    }
+    a.item_ctr = base[dev] + 2 * (next_slot++ % kCtrSlots);
+  }
   switch (a.hd) {
     case 64: return launch_hd<64>(a, s);
     case 128: return launch_hd<128>(a, s);
