@@ -27,8 +27,10 @@
  * Conventions shared by every entry point
  *   - All tensor arguments are DEVICE pointers owned by the caller; the
  *     library allocates no device memory and keeps no state between calls
- *     except a thread-local error message and one device-side error word
- *     (see g4_take_device_error).
+ *     except a thread-local error message, one device-side error word (see
+ *     g4_take_device_error), the built-in scratch of g4_attn_decode_noalloc
+ *     and 64 pairs of work-item counters of the bf16 prefill (see
+ *     g4_attn_prefill), all of them static device variables.
  *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL is the legacy default stream).  A call that returns G4_OK has only
  *     enqueued work.
@@ -164,7 +166,11 @@ g4_status g4_kv_append_normrope(const g4_layer_params* params, const g4_kv_cache
  * match the layer's type, head_dim, n_kv_heads and dtype
  * (G4_ERR_SHARE_MISMATCH otherwise).  bf16 runs on the tcgen05 tensor cores
  * (bf16 operands, float32 accumulation, P rounded to bf16); f32 runs on CUDA
- * cores in float32.
+ * cores in float32.  The bf16 kernel is persistent: its CTAs draw work items
+ * from a counter pair the library keeps in device memory, one of 64 taken in
+ * turn per call and cleared by the launch when it ends; so at most 64 bf16
+ * prefill launches may be in flight at the same time (any streams; a CUDA
+ * graph keeps the pair it was captured with).
  */
 g4_status g4_attn_prefill(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
                           int32_t layer, const void* q, const int32_t* q_start_pos, int32_t B, int32_t T,
