@@ -169,8 +169,10 @@ g4_status g4_kv_append_normrope(const g4_layer_params* params, const g4_kv_cache
  * cores in float32.  The bf16 kernel is persistent: its CTAs draw work items
  * from a counter pair the library keeps in device memory, one of 64 taken in
  * turn per call and cleared by the launch when it ends; so at most 64 bf16
- * prefill launches may be in flight at the same time (any streams; a CUDA
- * graph keeps the pair it was captured with).
+ * prefill launches may be in flight at the same time (any streams).  A CUDA
+ * graph keeps the pair it was captured with: replays of one graph, or of two
+ * graphs whose prefill captures were a multiple of 64 calls apart, must not
+ * overlap.
  */
 g4_status g4_attn_prefill(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
                           int32_t layer, const void* q, const int32_t* q_start_pos, int32_t B, int32_t T,
