@@ -189,8 +189,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   // 128-byte-swizzled tiles need 1024-byte alignment; the declaration asks
   // for it, and a block that does not get it reports and does nothing.
   extern __shared__ __align__(1024) uint8_t smem[];
+  // The last CTA to finish clears the launch's work-item counters for the
+  // next launch that uses them (every CTA has drawn its last item by then).
+  auto release_counters = [&]() {
+    if (threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(a.item_ctr + 1, 1u) == gridDim.x - 1) {
+        __threadfence();
+        atomicExch(a.item_ctr, 0u);
+        atomicExch(a.item_ctr + 1, 0u);
+      }
+    }
+  };
   if ((smem_u32(smem) & 1023u) != 0) {
     if (threadIdx.x == 0) atomicExch(a.err, kErrSmemAlign);
+    release_counters();
     return;
   }
   TcBars* bars = reinterpret_cast<TcBars*>(smem + C::BAR_OFF);
@@ -664,16 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-  // The last CTA to finish (every CTA has drawn its last item by now) clears
-  // the counters for the next launch that uses them.
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(a.item_ctr + 1, 1u) == gridDim.x - 1) {
-      __threadfence();
-      atomicExch(a.item_ctr, 0u);
-      atomicExch(a.item_ctr + 1, 0u);
-    }
-  }
+  release_counters();
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
