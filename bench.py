@@ -45,7 +45,7 @@ DECODE_EVENT_STEPS = (0, 32, 64, 96, 127)
 # DRAM bytes (read + write) per launch from one ncu capture of each kernel on
 # the 42-layer stack (profiles/*_stack42_bf16.md: dram__bytes.sum.per_second x
 # gpu__time_duration); the decode figures are for the first decode step.
-PROFILED_TRAFFIC = {"prefill_full": 637097472, "decode_full": 137716979, "decode_sliding": 8492032}
+PROFILED_TRAFFIC = {"prefill_full": 637334783, "decode_full": 137716979, "decode_sliding": 8492032}
 
 
 def parse_args(argv=None):
