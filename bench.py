@@ -43,7 +43,7 @@ WORKLOAD = "stack42_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DECODE_EVENT_STEPS = (0, 32, 64, 96, 127)
 # DRAM bytes (read + write) per launch from one ncu capture of each kernel on
-# the 42-layer stack (profiles/*_stack42_bf16.md: dram__bytes.sum.per_second x
+# the 42-layer stack with an 8-step decode phase (dram__bytes.sum.per_second x
 # gpu__time_duration); the decode figures are for the first decode step.
 PROFILED_TRAFFIC = {"prefill_full": 637334783, "decode_full": 137716979, "decode_sliding": 8492032}
 
@@ -407,7 +407,7 @@ def run_ours(args, cfg):
                       peak_kind=f"{peak_src} bf16 dense, sustained (timed inside a long step)",
                       flops_per_launch=pf_flops, avg_launch_ms=pf_avg * 1e3, launches_sampled=len(pf_launch),
                       launches_per_step=len(job.full_layers), traffic=PROFILED_TRAFFIC["prefill_full"],
-                      traffic_source="profiles/prefill_tc_full512_stack42_bf16.md")
+                      traffic_source="ncu capture, 42-layer stack, layer 5")
     rl_prefill["frac"] = rl_prefill["achieved"] / rl_prefill["peak"]
     rooflines = [rl_prefill]
     kinds = (("full", job.full_layers, "attn_simt_kernel<bf16,512,4,fused> (full-layer decode step: append + "
@@ -428,8 +428,8 @@ def run_ours(args, cfg):
                       avg_launch_ms=avg_t * 1e3, launches_sampled=n_launches,
                       launches_per_step=len(layers) * cfg["decode_steps"],
                       traffic=PROFILED_TRAFFIC["decode_" + kind],
-                      traffic_source=f"profiles/decode_step_{'full512' if kind == 'full' else 'sliding256'}"
-                                     "_stack42_bf16.md (first decode step)",
+                      traffic_source=f"ncu capture, 42-layer stack, layer {'5' if kind == 'full' else '0'}, "
+                                     "first decode step",
                       per_launch_gbs_min=min(per) / 1e9, per_launch_gbs_max=max(per) / 1e9)
         rl_dec["frac"] = rl_dec["achieved"] / rl_dec["peak"]
         if kind == "sliding":
