@@ -29,6 +29,12 @@ What it computes, and where each step comes from (page title + function):
                         scale 1.0 and ``window``; ferrox-models
                         ``causal_gqa_attention[_windowed]``; head grouping as in
                         taconite ``text_attention``: ``kh = hh / group``).
+* ``ring_rows``      -- sliding-window ring-buffer cache: a sliding layer's
+                        cache of capacity C keeps position p in row p mod C,
+                        so only the last C positions stay resident
+                        (turbospark-runtime ``gemma4`` decode: ``ring_capacity``
+                        and ``active_ring`` passed to the attention next to
+                        ``kv_start = seq_len - sliding_window``).
 * ``kv_share_src``   -- shared-KV routing of the tail layers
                         (ferrox-models ``Gemma4Hparams::kv_reuse_layer``;
                         cortiq-engine ``g4e.rs`` module doc on shared KV).
@@ -183,7 +189,7 @@ def normrope_kv(k_in, v_in, k_norm_w, positions, head_dim, theta, rotary_fractio
     return kn, vn
 
 
-def kv_append_normrope(lp, q_in, k_in, v_in, q_norm_w, k_norm_w, positions, cache_k, cache_v):
+def kv_append_normrope(lp, q_in, k_in, v_in, q_norm_w, k_norm_w, positions, cache_k, cache_v, ring=False):
     """Step a4 for one layer and a batch of tokens.
 
     lp: dict with head_dim, theta, rotary_fraction, eps, dtype and
@@ -191,7 +197,8 @@ def kv_append_normrope(lp, q_in, k_in, v_in, q_norm_w, k_norm_w, positions, cach
     q_in [B, T, H, hd]; k_in / v_in [B, T, Hkv, hd] or None on a shared
     layer; positions [B, T] (the cache slot and the RoPE position);
     cache_k / cache_v [B, Hkv, Lmax, hd] float64 arrays updated in place
-    (ignored on a shared layer).
+    (ignored on a shared layer).  With ``ring`` the cache is a sliding-window
+    ring of Lmax rows and position p goes to row p mod Lmax (``ring_rows``).
 
     Returns q_out [B, T, H, hd] as stored (bf16- or f32-rounded).
     Shared layers norm and rope q and write nothing
@@ -206,12 +213,58 @@ def kv_append_normrope(lp, q_in, k_in, v_in, q_norm_w, k_norm_w, positions, cach
         kn = store(kn, dt)
         vn = store(vn, dt)
         B, T = positions.shape
+        cap = cache_k.shape[2]
         for b in range(B):
             for t in range(T):
-                p = positions[b, t]
-                cache_k[b, :, p, :] = kn[b, t]
-                cache_v[b, :, p, :] = vn[b, t]
+                p = int(positions[b, t])
+                row = ring_slot(p, cap) if ring else p
+                cache_k[b, :, row, :] = kn[b, t]
+                cache_v[b, :, row, :] = vn[b, t]
     return q_out
+
+
+# --------------------------------------------------------------------------
+# Sliding-window ring-buffer cache
+# --------------------------------------------------------------------------
+
+def ring_slot(pos, capacity):
+    """Row of a ring cache of ``capacity`` rows that holds position ``pos``.
+
+    The ring keeps every position in row pos mod capacity, so appending
+    position p overwrites position p - capacity (turbospark-runtime
+    ``gemma4`` decode: the attention gets the ring capacity once the sequence
+    is longer than it, ``if ring > 0 && seq_len > ring``).
+    """
+    if capacity < 1 or pos < 0:
+        raise ValueError("ring capacity must be >= 1 and positions >= 0")
+    return pos % capacity
+
+
+def ring_rows(kv_len, capacity):
+    """Positions still resident in a ring after positions [0, kv_len) were
+    appended in order, and the rows holding them: the last ``capacity``
+    positions, (positions, rows) in position order."""
+    pos = np.arange(max(0, kv_len - capacity), kv_len, dtype=np.int64)
+    return pos, pos % capacity
+
+
+def check_ring_covers(q_pos, kv_len, capacity, layer_type, window):
+    """Raise unless every key a query needs is still resident in the ring.
+
+    Only a sliding layer can use a ring (a full layer needs every earlier
+    key).  The query at q_pos needs positions [max(0, q_pos - window + 1),
+    q_pos]; the ring holds [max(0, kv_len - capacity), kv_len).  So a chunk
+    of T new tokens appended before its attention needs
+    capacity >= T + window - 1.
+    """
+    if layer_type != SLIDING:
+        raise ValueError("a ring cache needs a sliding layer")
+    first_resident = max(0, int(kv_len) - capacity)
+    q_pos = np.asarray(q_pos, dtype=np.int64)
+    need = np.maximum(0, q_pos - window + 1)
+    if np.any(need < first_resident):
+        raise ValueError("ring of %d rows no longer holds key %d that a query needs"
+                         % (capacity, int(np.min(need))))
 
 
 # --------------------------------------------------------------------------
@@ -249,12 +302,22 @@ def attention_probs(q_row, keys, k_pos, q_pos, layer_type, window, scale):
     return e / np.sum(e)
 
 
-def attention(q, cache_k, cache_v, q_pos, kv_len, n_kv_heads, layer_type, window, scale=1.0):
+def key_rows(kv_len, capacity, ring):
+    """(positions, cache rows) of the keys a sequence of kv_len tokens has:
+    rows 0 .. kv_len-1 of a linear cache, the resident part of a ring."""
+    if ring:
+        return ring_rows(kv_len, capacity)
+    pos = np.arange(kv_len, dtype=np.int64)
+    return pos, pos
+
+
+def attention(q, cache_k, cache_v, q_pos, kv_len, n_kv_heads, layer_type, window, scale=1.0, ring=False):
     """o[b, t, h] = sum_j softmax_j(scale * q[b,t,h] . k_j) v_j over visible j.
 
     q [B, T, H, hd] (already normed and roped); cache_k / cache_v
     [B, Hkv, Lmax, hd]; q_pos [B, T] positions of the queries; kv_len [B]
-    number of cache rows holding keys (rows >= kv_len are never read).
+    number of positions holding keys (rows >= kv_len of a linear cache are
+    never read; a ring cache, ``ring``, holds the last Lmax of them).
     Query head h reads kv head h // (H / Hkv).  Returns float64 [B, T, H, hd].
     """
     q = np.asarray(q, dtype=np.float64)
@@ -262,14 +325,17 @@ def attention(q, cache_k, cache_v, q_pos, kv_len, n_kv_heads, layer_type, window
     g = H // n_kv_heads
     out = np.zeros((B, T, H, hd), dtype=np.float64)
     q_pos = np.asarray(q_pos, dtype=np.int64)
+    cap = cache_k.shape[2]
     for b in range(B):
         L = int(kv_len[b])
-        j = np.arange(L)
-        vis = visible(q_pos[b][:, None], j[None, :], layer_type, window)   # [T, L]
+        if ring:
+            check_ring_covers(q_pos[b], L, cap, layer_type, window)
+        j, rows = key_rows(L, cap, ring)
+        vis = visible(q_pos[b][:, None], j[None, :], layer_type, window)   # [T, keys]
         for h in range(H):
             kvh = h // g
-            K = np.asarray(cache_k[b, kvh, :L], dtype=np.float64)
-            V = np.asarray(cache_v[b, kvh, :L], dtype=np.float64)
+            K = np.asarray(cache_k[b, kvh, rows], dtype=np.float64)
+            V = np.asarray(cache_v[b, kvh, rows], dtype=np.float64)
             S = (q[b, :, h, :] @ K.T) * scale
             S = np.where(vis, S, -np.inf)
             m = np.max(S, axis=1, keepdims=True)
@@ -279,7 +345,8 @@ def attention(q, cache_k, cache_v, q_pos, kv_len, n_kv_heads, layer_type, window
     return out
 
 
-def attention_rows(q, cache_k, cache_v, rows, q_pos, kv_len, n_kv_heads, layer_type, window, scale=1.0):
+def attention_rows(q, cache_k, cache_v, rows, q_pos, kv_len, n_kv_heads, layer_type, window, scale=1.0,
+                   ring=False):
     """The same definition evaluated one output row at a time.
 
     rows: iterable of (b, t, h).  Returns float64 [len(rows), hd].  Used where
@@ -288,13 +355,17 @@ def attention_rows(q, cache_k, cache_v, rows, q_pos, kv_len, n_kv_heads, layer_t
     q = np.asarray(q)
     H = q.shape[2]
     g = H // n_kv_heads
+    cap = cache_k.shape[2]
     res = []
     for (b, t, h) in rows:
         L = int(kv_len[b])
         kvh = h // g
-        K = np.asarray(cache_k[b, kvh, :L], dtype=np.float64)
-        V = np.asarray(cache_v[b, kvh, :L], dtype=np.float64)
-        p = attention_probs(q[b, t, h], K, np.arange(L), int(q_pos[b, t]), layer_type, window, scale)
+        if ring:
+            check_ring_covers(q_pos[b, t], L, cap, layer_type, window)
+        j, crow = key_rows(L, cap, ring)
+        K = np.asarray(cache_k[b, kvh, crow], dtype=np.float64)
+        V = np.asarray(cache_v[b, kvh, crow], dtype=np.float64)
+        p = attention_probs(q[b, t, h], K, j, int(q_pos[b, t]), layer_type, window, scale)
         res.append(p @ V)
     return np.stack(res) if res else np.zeros((0, q.shape[-1]))
 

@@ -402,3 +402,112 @@ def test_stack_shared_layer_reads_source_cache():
         ck, cv = caches[lp["kv_share_src"]]
         direct = O.store(O.attention(qn, ck, cv, pos, [T], Hkv, lp["layer_type"], lp["window"]), lp["dtype"])
         assert np.array_equal(outs[li], direct)
+
+
+# ------------------------------------------------- sliding-window ring cache
+
+def test_ring_rows_keep_the_last_capacity_positions():
+    # A FIFO of bounded length is an independent model of "the ring keeps the
+    # last C positions": after each append its content must be exactly the
+    # resident set the oracle reports, each held in a distinct row.
+    import collections
+    for cap in (1, 3, 5, 8):
+        fifo = collections.deque(maxlen=cap)
+        for n in range(1, 4 * cap + 3):
+            fifo.append(n - 1)
+            pos, rows = O.ring_rows(n, cap)
+            assert list(pos) == list(fifo)
+            assert len(set(rows.tolist())) == len(rows)
+            assert all(0 <= r < cap for r in rows)
+            # the row the newest position went to is the one it overwrote
+            if n > cap:
+                assert O.ring_slot(n - 1, cap) == O.ring_slot(n - 1 - cap, cap)
+
+
+def test_ring_append_holds_what_a_linear_cache_holds():
+    # Appending the same tokens in chunks to a linear cache and to a ring of
+    # capacity C: every resident position's row in the ring is bit-equal to
+    # that position's row in the linear cache (same arithmetic, other slot).
+    B, Hkv, H, hd, cap, N = 2, 2, 4, 64, 7, 19
+    r = rng(31)
+    lp = dict(head_dim=hd, theta=1e4, rotary_fraction=1.0, eps=1e-6, dtype=O.BF16, kv_share_src=-1)
+    q = r.standard_normal((B, N, H, hd))
+    k = r.standard_normal((B, N, Hkv, hd))
+    v = r.standard_normal((B, N, Hkv, hd))
+    qw = 1 + 0.1 * r.standard_normal(hd)
+    kw = 1 + 0.1 * r.standard_normal(hd)
+    lin_k = np.zeros((B, Hkv, N, hd))
+    lin_v = np.zeros((B, Hkv, N, hd))
+    ring_k = np.full((B, Hkv, cap, hd), 99.0)
+    ring_v = np.full((B, Hkv, cap, hd), 99.0)
+    start = 0
+    for T in (5, 1, 1, 6, 1, 5):
+        sl = slice(start, start + T)
+        pos = np.broadcast_to(np.arange(start, start + T)[None, :], (B, T))
+        q1 = O.kv_append_normrope(lp, q[:, sl], k[:, sl], v[:, sl], qw, kw, pos, lin_k, lin_v)
+        q2 = O.kv_append_normrope(lp, q[:, sl], k[:, sl], v[:, sl], qw, kw, pos, ring_k, ring_v, ring=True)
+        assert np.array_equal(q1, q2)
+        start += T
+        rpos, rrows = O.ring_rows(start, cap)
+        for p, row in zip(rpos, rrows):
+            assert np.array_equal(ring_k[:, :, row], lin_k[:, :, p])
+            assert np.array_equal(ring_v[:, :, row], lin_v[:, :, p])
+        # rows not yet reached keep their old content
+        for row in range(start, cap):
+            assert np.all(ring_k[:, :, row] == 99.0)
+    assert start == N
+
+
+@pytest.mark.parametrize("window,extra", [(4, 0), (4, 3), (1, 0)])
+def test_ring_attention_equals_linear_attention(window, extra):
+    # Prefill chunks and single-token decode steps on a sliding layer: with a
+    # ring of capacity T_chunk + W - 1 (+ extra) the attention output equals
+    # the one on a linear cache holding every position (the linear form is
+    # pinned above by SDPA and by brute-force loops).  Not bitwise: the ring
+    # form sums over fewer masked (zero) terms.
+    B, Hkv, H, hd = 2, 2, 4, 64
+    chunks = (6, 1, 1, 1, 6, 2, 1)
+    N = sum(chunks)
+    cap = max(chunks) + window - 1 + extra
+    r = rng(32 + window + extra)
+    lp = dict(head_dim=hd, theta=1e4, rotary_fraction=1.0, eps=1e-6, dtype=O.F32, kv_share_src=-1)
+    q = r.standard_normal((B, N, H, hd))
+    k = r.standard_normal((B, N, Hkv, hd))
+    v = r.standard_normal((B, N, Hkv, hd))
+    qw = 1 + 0.1 * r.standard_normal(hd)
+    kw = 1 + 0.1 * r.standard_normal(hd)
+    lin = (np.zeros((B, Hkv, N, hd)), np.zeros((B, Hkv, N, hd)))
+    ring = (np.full((B, Hkv, cap, hd), np.nan), np.full((B, Hkv, cap, hd), np.nan))
+    start = 0
+    for T in chunks:
+        sl = slice(start, start + T)
+        pos = np.broadcast_to(np.arange(start, start + T)[None, :], (B, T))
+        qo = O.kv_append_normrope(lp, q[:, sl], k[:, sl], v[:, sl], qw, kw, pos, *lin)
+        O.kv_append_normrope(lp, q[:, sl], k[:, sl], v[:, sl], qw, kw, pos, *ring, ring=True)
+        start += T
+        kv_len = np.full(B, start)
+        o_lin = O.attention(qo, *lin, pos, kv_len, Hkv, O.SLIDING, window)
+        o_ring = O.attention(qo, *ring, pos, kv_len, Hkv, O.SLIDING, window, ring=True)
+        assert np.all(np.isfinite(o_ring))
+        np.testing.assert_allclose(o_ring, o_lin, rtol=0, atol=1e-12)
+        rows = [(b, t, h) for b in range(B) for t in range(T) for h in range(H)]
+        o_rows = O.attention_rows(qo, *ring, rows, pos, kv_len, Hkv, O.SLIDING, window, ring=True)
+        np.testing.assert_allclose(o_rows, o_lin.reshape(-1, hd), rtol=0, atol=1e-12)
+
+
+def test_ring_too_small_or_on_a_full_layer_is_refused():
+    B, Hkv, H, hd, W, T = 1, 1, 1, 64, 4, 5
+    r = rng(33)
+    q = r.standard_normal((B, T, H, hd))
+    cap = T + W - 2  # one row short: the first query's oldest key is gone
+    ck = r.standard_normal((B, Hkv, cap, hd))
+    pos = np.arange(10, 10 + T)[None, :]
+    with pytest.raises(ValueError):
+        O.attention(q, ck, ck, pos, [10 + T], Hkv, O.SLIDING, W, ring=True)
+    # one more row suffices
+    ck2 = r.standard_normal((B, Hkv, cap + 1, hd))
+    O.attention(q, ck2, ck2, pos, [10 + T], Hkv, O.SLIDING, W, ring=True)
+    with pytest.raises(ValueError):
+        O.attention(q, ck2, ck2, pos, [10 + T], Hkv, O.FULL, W, ring=True)
+    with pytest.raises(ValueError):
+        O.ring_slot(-1, 4)
