@@ -97,6 +97,16 @@ g4_status resolve_src(const g4_layer_params* p, const g4_kv_cache* caches, int n
                 layer, p->layer_type, p->head_dim, p->n_kv_heads, p->dtype, src, c->layer_type, c->head_dim,
                 c->n_kv_heads, c->dtype);
   if (c->max_len < 1 || c->batch < 1) return fail(G4_ERR_INVALID_ARG, "cache of layer %d has no rows", src);
+  if (c->ring != 0 && c->ring != 1) return fail(G4_ERR_INVALID_ARG, "cache of layer %d: ring %d is neither 0 nor 1", src, c->ring);
+  if (c->ring) {
+    // A ring keeps the last max_len positions: only a sliding layer's window
+    // fits in one, and the window itself must fit.
+    if (c->layer_type != G4_SLIDING)
+      return fail(G4_ERR_INVALID_ARG, "cache of layer %d is a ring but not a sliding layer's", src);
+    if (c->max_len < p->window)
+      return fail(G4_ERR_CAPACITY, "ring cache of layer %d has %d rows, fewer than the window %d", src, c->max_len,
+                  p->window);
+  }
   if (!aligned16(c->k) || !aligned16(c->v))
     return fail(G4_ERR_INVALID_ARG, "cache of layer %d is not 16-byte aligned", src);
   *out = c;
@@ -181,6 +191,7 @@ g4_status g4_kv_append_normrope(const g4_layer_params* params, const g4_kv_cache
     a.cache_k = c->k;
     a.cache_v = c->v;
     a.max_len = c->max_len;
+    a.ring = c->ring;
     a.k_in = k_in;
     a.v_in = v_in;
     a.k_w = k_norm_w;
@@ -225,7 +236,18 @@ g4_status g4_attn_prefill(const g4_layer_params* params, const g4_kv_cache* cach
   st = resolve_src(params, caches, n_layers, layer, &c);
   if (st != G4_OK) return st;
   if (c->batch < B) return fail(G4_ERR_CAPACITY, "cache batch %d < B %d", c->batch, B);
-  if (T > c->max_len) return fail(G4_ERR_CAPACITY, "T %d exceeds the cache length %d", T, c->max_len);
+  if (c->ring) {
+    // Every key of the chunk's windows must still be in the ring after the
+    // chunk's own T rows went in: T + window - 1 positions.
+    if (static_cast<long long>(T) + params->window - 1 > c->max_len)
+      return fail(G4_ERR_CAPACITY, "ring cache of %d rows cannot hold the %d + %d - 1 keys a chunk of T = %d needs",
+                  c->max_len, T, params->window, T);
+    if (params->dtype == G4_BF16 && c->max_len % 128 != 0)
+      return fail(G4_ERR_UNSUPPORTED, "bf16 prefill on a ring cache needs max_len a multiple of 128 (got %d)",
+                  c->max_len);
+  } else if (T > c->max_len) {
+    return fail(G4_ERR_CAPACITY, "T %d exceeds the cache length %d", T, c->max_len);
+  }
   if (B == 0 || T == 0) return ok();
   int* err = device_error_ptr();
   if (err == nullptr) return fail(G4_ERR_CUDA, "cannot resolve the device error word");
@@ -245,6 +267,7 @@ g4_status g4_attn_prefill(const g4_layer_params* params, const g4_kv_cache* cach
     a.Hkv = params->n_kv_heads;
     a.hd = params->head_dim;
     a.max_len = c->max_len;
+    a.ring = c->ring;
     a.sliding = params->layer_type == G4_SLIDING;
     a.window = params->window;
     a.scale_log2 = scale_log2;
@@ -265,6 +288,7 @@ g4_status g4_attn_prefill(const g4_layer_params* params, const g4_kv_cache* cach
   a.Hkv = params->n_kv_heads;
   a.hd = params->head_dim;
   a.max_len = c->max_len;
+  a.ring = c->ring;
   a.sliding = params->layer_type == G4_SLIDING;
   a.window = params->window;
   a.len_cap = c->max_len;
@@ -314,7 +338,7 @@ g4_status decode_common(const g4_layer_params* params, const g4_kv_cache* caches
   st = resolve_src(params, caches, n_layers, layer, &c);
   if (st != G4_OK) return st;
   if (c->batch < B) return fail(G4_ERR_CAPACITY, "cache batch %d < B %d", c->batch, B);
-  if (max_seq_len < 1 || max_seq_len > c->max_len)
+  if (max_seq_len < 1 || (!c->ring && max_seq_len > c->max_len))
     return fail(G4_ERR_CAPACITY, "max_seq_len %d outside [1, cache length %d]", max_seq_len, c->max_len);
   if (B == 0) return ok();
   const g4::DecodePlan plan = g4::decode_plan(params->layer_type == G4_SLIDING, params->window, params->head_dim,
@@ -340,6 +364,7 @@ g4_status decode_common(const g4_layer_params* params, const g4_kv_cache* caches
   a.Hkv = params->n_kv_heads;
   a.hd = params->head_dim;
   a.max_len = c->max_len;
+  a.ring = c->ring;
   a.sliding = params->layer_type == G4_SLIDING;
   a.window = params->window;
   a.len_cap = max_seq_len;

@@ -208,10 +208,13 @@ __global__ void __launch_bounds__(128, HD >= 512 ? 5 : 8) append_normrope_kernel
     } else {
       const bool is_k = row < a.H + a.Hkv;
       const int kvh = is_k ? row - a.H : row - a.H - a.Hkv;
-      rr.valid = pos >= 0 && pos < a.max_len;  // k / v need a cache slot
+      // k / v need a cache row: the position itself, or on a sliding-window
+      // ring the position modulo its capacity.
+      rr.valid = pos >= 0 && (a.ring || pos < a.max_len);
+      const int crow = !rr.valid ? 0 : (a.ring ? pos % a.max_len : pos);
       rr.src = static_cast<const T*>(is_k ? a.k_in : a.v_in) + (static_cast<size_t>(tok) * a.Hkv + kvh) * HD;
       rr.dst = static_cast<T*>(is_k ? a.cache_k : a.cache_v) +
-               ((static_cast<size_t>(b) * a.Hkv + kvh) * a.max_len + (rr.valid ? pos : 0)) * HD;
+               ((static_cast<size_t>(b) * a.Hkv + kvh) * a.max_len + crow) * HD;
       rr.w = is_k ? a.k_w : nullptr;
       rr.rope = is_k;
     }

@@ -323,6 +323,8 @@ __global__ void __launch_bounds__(NW * 32, (SimtCfg<T, HD, G, NW>::MINB))
   int L;
   if (a.mode == 0) {
     L = min(max(a.base[b], 1), a.len_cap);
+  } else if (a.ring) {
+    L = max(a.base[b] + t, 0) + 1;  // every position has a row in a ring
   } else {
     L = min(max(a.base[b] + t, 0), a.max_len - 1) + 1;
   }
@@ -355,9 +357,25 @@ __global__ void __launch_bounds__(NW * 32, (SimtCfg<T, HD, G, NW>::MINB))
     const uint32_t bytes = static_cast<uint32_t>(n) * C::ROWB;
     const uint32_t bar = smem_u32(&bars[w * C::NST + buf]);
     uint8_t* rw = smem + w * (C::NST * 2 * C::STAGE_B);
+    const uint32_t dk = smem_u32(rw + buf * 2 * C::STAGE_B);
+    const uint32_t dv = dk + C::STAGE_B;
     mbar_arrive_expect_tx(bar, 2 * bytes);
-    bulk_g2s(smem_u32(rw + buf * 2 * C::STAGE_B), gk + static_cast<size_t>(kk0) * HD, bytes, bar);
-    bulk_g2s(smem_u32(rw + buf * 2 * C::STAGE_B + C::STAGE_B), gv + static_cast<size_t>(kk0) * HD, bytes, bar);
+    if (!a.ring) {
+      bulk_g2s(dk, gk + static_cast<size_t>(kk0) * HD, bytes, bar);
+      bulk_g2s(dv, gv + static_cast<size_t>(kk0) * HD, bytes, bar);
+    } else {
+      // Positions kk0 .. kk0+n-1 sit in rows r0 .. (wrapping to row 0 once
+      // the ring's end is reached, at most once since n <= max_len).
+      const int r0 = kk0 % a.max_len;
+      const int n0 = min(n, a.max_len - r0);
+      const uint32_t b0 = static_cast<uint32_t>(n0) * C::ROWB;
+      bulk_g2s(dk, gk + static_cast<size_t>(r0) * HD, b0, bar);
+      bulk_g2s(dv, gv + static_cast<size_t>(r0) * HD, b0, bar);
+      if (n0 < n) {
+        bulk_g2s(dk + b0, gk, bytes - b0, bar);
+        bulk_g2s(dv + b0, gv, bytes - b0, bar);
+      }
+    }
   };
   auto issue = [&](int st_idx, int buf) { issue_for(warp, st_idx, buf); };
 
@@ -396,7 +414,8 @@ __global__ void __launch_bounds__(NW * 32, (SimtCfg<T, HD, G, NW>::MINB))
       } else {
         const bool is_k = job == G;
         j.src = static_cast<const T*>(is_k ? a.k_raw : a.v_raw) + (static_cast<size_t>(b) * a.Hkv + kvh) * HD;
-        j.dst_g = static_cast<T*>(is_k ? a.cache_k : a.cache_v) + (head_base + (L - 1)) * HD;
+        const int row = a.ring ? (L - 1) % a.max_len : L - 1;
+        j.dst_g = static_cast<T*>(is_k ? a.cache_k : a.cache_v) + (head_base + row) * HD;
         j.w = is_k ? a.k_w : nullptr;
         j.rope = is_k;
       }

@@ -22,6 +22,7 @@ struct AppendArgs {
   void* cache_k;  // [B][Hkv][max_len][hd]
   void* cache_v;
   int B, T, H, Hkv, hd, max_len;
+  int ring;          // 1: position p goes to row p mod max_len (sliding-window ring)
   int rows_per_cta;  // head rows (of H + 2 Hkv) handled per CTA
   int tok_per_cta;   // tokens (same t, consecutive b) handled per CTA
   int n_rot;         // rotated pairs; inv_freq[j] == 0 for j >= n_rot
@@ -51,6 +52,7 @@ struct AttnSimtArgs {
   int* err;
   int mode;
   int B, T, H, Hkv, hd, max_len;
+  int ring;         // 1: key position p is row p mod max_len (sliding-window ring)
   int sliding, window;
   int len_cap;      // decode: lengths clamped to [1, len_cap]
   int chunk;        // keys per split
@@ -79,6 +81,7 @@ struct PrefillTcArgs {
   const int32_t* q_start;  // [B]
   int* err;
   int B, T, H, Hkv, hd, max_len;
+  int ring;          // 1: key position p is row p mod max_len (max_len a multiple of 128)
   int sliding, window;
   float scale_log2;
   unsigned* item_ctr;  // [2]: next work item, CTAs done (zero between launches; set by the launcher)

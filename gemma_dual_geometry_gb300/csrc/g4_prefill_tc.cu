@@ -172,7 +172,8 @@ __device__ __forceinline__ TcItem tc_item(const PrefillTcArgs& a, int it, int nq
   w.valid_rows = min(kBM, a.T - w.q0);
   w.qpos_first = q_start + w.q0;
   const int qpos_last = w.qpos_first + w.valid_rows - 1;
-  w.Lk = min(q_start + a.T, a.max_len);  // cache rows holding keys
+  // keys held: positions [0, Lk) (a ring holds the last max_len of them)
+  w.Lk = a.ring ? q_start + a.T : min(q_start + a.T, a.max_len);
   const int kend = min(qpos_last + 1, w.Lk);
   const int kbeg = a.sliding ? max(0, w.qpos_first - a.window + 1) : 0;
   w.kt_begin = kbeg / kBN;
@@ -292,21 +293,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int r = 0; r < QREQ; ++r)
           tma_load_5d(sQ + r * (C::QCH / QREQ) * kChunkB, &tm_q, 0, w.q0, r * (C::QCH / QREQ), w.h, w.b, qb);
         ++nq;
+        // Cache row of a key tile's first position: on a ring of max_len
+        // rows (a multiple of the 128-key tile, so no tile wraps) the
+        // position modulo max_len.
+        auto tile_row = [&](int kt) { return a.ring ? (kt * kBN) % a.max_len : kt * kBN; };
         auto load_k = [&](int kt) {
+          const int kr = tile_row(kt);
           for (int p2 = 0; p2 < C::KPARTS && ok; ++p2) {
             if (!thread_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, a.err, abort)) { ok = false; break; }
             const uint32_t fb = smem_u32(&bars->full[slot]);
             mbar_arrive_expect_tx(fb, C::KPB);
-            tma_load_5d(sRing + slot * C::SLOTB, &tm_k, 0, kt * kBN, p2 * C::CPP, w.kvh, w.b, fb);
+            tma_load_5d(sRing + slot * C::SLOTB, &tm_k, 0, kr, p2 * C::CPP, w.kvh, w.b, fb);
             advance();
           }
         };
         auto load_v = [&](int kt) {
+          const int kr = tile_row(kt);
           for (int p2 = 0; p2 < C::VPARTS && ok; ++p2) {
             if (!thread_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, a.err, abort)) { ok = false; break; }
             const uint32_t fb = smem_u32(&bars->full[slot]);
             mbar_arrive_expect_tx(fb, C::VPB);
-            tma_load_5d(sRing + slot * C::SLOTB, &tm_v, 0, kt * kBN + p2 * C::VKP, w.dh * (C::DV / 64), w.kvh, w.b,
+            tma_load_5d(sRing + slot * C::SLOTB, &tm_v, 0, kr + p2 * C::VKP, w.dh * (C::DV / 64), w.kvh, w.b,
                         fb);
             advance();
           }

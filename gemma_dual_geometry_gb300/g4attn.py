@@ -38,7 +38,7 @@ class G4LayerParams(ctypes.Structure):
 class G4KVCache(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("layer_type", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32), ("max_len", ctypes.c_int32),
-                ("batch", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("batch", ctypes.c_int32), ("dtype", ctypes.c_int32), ("ring", ctypes.c_int32)]
 
 
 _P = ctypes.POINTER
@@ -119,9 +119,10 @@ def cache_table(n_layers):
     return (G4KVCache * n_layers)()
 
 
-def set_cache(table, layer, k, v, layer_type, head_dim, n_kv_heads, max_len, batch, dtype):
+def set_cache(table, layer, k, v, layer_type, head_dim, n_kv_heads, max_len, batch, dtype, ring=False):
+    """Fill entry ``layer``; ``ring`` makes it a sliding-window ring of max_len rows."""
     table[layer] = G4KVCache(_ptr(k), _ptr(v), int(layer_type), int(head_dim), int(n_kv_heads), int(max_len),
-                             int(batch), int(dtype))
+                             int(batch), int(dtype), int(bool(ring)))
 
 
 def g4_kv_share_src(n_layers, n_shared, is_sliding, layer):

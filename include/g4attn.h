@@ -109,8 +109,16 @@ typedef struct {
 /*
  * One layer's KV cache, caller-owned device memory, layout
  * k[batch][n_kv_heads][max_len][head_dim] (same for v): rows of head_dim
- * contiguous, one row per token position.  Layers that read another layer's
- * cache may leave their entry zeroed.
+ * contiguous.  Layers that read another layer's cache may leave their entry
+ * zeroed.
+ *   ring = 0  linear cache: position p lives in row p, positions < max_len.
+ *   ring = 1  sliding-window ring buffer (turbospark-runtime gemma4 decode:
+ *             `ring_capacity`, `active_ring`): position p lives in row
+ *             p mod max_len, any p >= 0, so the cache keeps the last max_len
+ *             positions.  Only on a G4_SLIDING cache, with max_len >= the
+ *             layer's window (G4_ERR_INVALID_ARG / G4_ERR_CAPACITY otherwise).
+ *             A ring of `window` rows serves decode; a prefill chunk of T
+ *             tokens needs max_len >= T + window - 1 (see g4_attn_prefill).
  */
 typedef struct {
   void* k;
@@ -121,6 +129,7 @@ typedef struct {
   int32_t max_len;
   int32_t batch;
   int32_t dtype;
+  int32_t ring;
 } g4_kv_cache;
 
 /*
@@ -143,11 +152,14 @@ int32_t g4_kv_share_src(int32_t n_layers, int32_t n_shared, const int32_t* is_sl
  *   k_norm_w   [head_dim] float32 weight shared by all k heads (NULL on a
  *              shared layer).  v has no weight.
  *   positions  [B][T] int32: the RoPE position of each token and the cache row
- *              it is written to.  Rows outside [0, max_len) are not written.
+ *              it is written to (row = position on a linear cache, position
+ *              mod max_len on a ring).  Negative positions, and positions
+ *              >= max_len of a linear cache, are not written.
  *   q_out      [B][T][n_heads][head_dim] normed + roped q; may equal q_in.
  * The layer's cache is caches[layer] (n_layers entries).  Writes exactly the
- * rows k[b][*][positions[b][t]][*] and v[...] for every (b, t); nothing else
- * in the cache changes.  RoPE angles are pos * inv_freq[j] with inv_freq held
+ * rows k[b][*][row(positions[b][t])][*] and v[...] for every (b, t); nothing
+ * else in the cache changes.  Two tokens of one call that map to the same
+ * ring row leave either one there.  RoPE angles are pos * inv_freq[j] with inv_freq held
  * in float32 and the angle reduced in float64.
  */
 g4_status g4_kv_append_normrope(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
@@ -160,7 +172,11 @@ g4_status g4_kv_append_normrope(const g4_layer_params* params, const g4_kv_cache
  *   q            [B][T][n_heads][head_dim], normed + roped (g4_kv_append_normrope's q_out)
  *   q_start_pos  [B] int32 device: token t of sequence b sits at position
  *                q_start_pos[b] + t; the cache of the source layer must
- *                already hold rows [0, q_start_pos[b] + T)
+ *                already hold positions [0, q_start_pos[b] + T).  On a ring
+ *                cache those are the last max_len of them, and every key the
+ *                chunk needs is still there when max_len >= T + window - 1
+ *                (checked: G4_ERR_CAPACITY); a bf16 ring also needs max_len
+ *                a multiple of 128, the key tile (G4_ERR_UNSUPPORTED).
  *   out          [B][T][n_heads][head_dim]
  * Reads caches[src], src = kv_share_src < 0 ? layer : kv_share_src, which must
  * match the layer's type, head_dim, n_kv_heads and dtype
@@ -190,8 +206,9 @@ size_t g4_attn_decode_workspace_size(const g4_layer_params* params, int32_t B, i
  *   seq_lens     [B] int32 device: keys per sequence INCLUDING the new token,
  *                which sits at position seq_lens[b] - 1 (append it first).
  *                Values are clamped into [1, max_seq_len].
- *   max_seq_len  host-side upper bound of seq_lens, 1..cache max_len; it sizes
- *                the split-KV grid and the workspace.
+ *   max_seq_len  host-side upper bound of seq_lens, 1..cache max_len (any
+ *                value >= 1 on a ring cache); it sizes the split-KV grid and
+ *                the workspace.
  *   out          [B][n_heads][head_dim]
  *   workspace    device scratch of at least g4_attn_decode_workspace_size()
  *                bytes (may be NULL when that is 0); caller-owned, 16-byte
@@ -214,8 +231,10 @@ g4_status g4_attn_decode(const g4_layer_params* params, const g4_kv_cache* cache
  *   q_in         [B][n_heads][head_dim] raw q of the new token
  *   k_in, v_in   [B][n_kv_heads][head_dim] raw k / v (NULL on a shared layer)
  *   q_norm_w, k_norm_w  float32 [head_dim] (k_norm_w NULL on a shared layer)
- * On a layer that owns its cache the new k / v rows are written to row
- * seq_lens[b] - 1 of caches[layer].  Other arguments as g4_attn_decode.
+ * On a layer that owns its cache the new k / v rows are written to position
+ * seq_lens[b] - 1 of caches[layer] (row seq_lens[b] - 1, or that mod max_len
+ * on a ring, which overwrites a key the window no longer sees).  Other
+ * arguments as g4_attn_decode.
  */
 g4_status g4_decode_step(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers, int32_t layer,
                          const void* q_in, const void* k_in, const void* v_in, const float* q_norm_w,

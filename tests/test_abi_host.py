@@ -178,6 +178,50 @@ def test_decode_step_validation(L):
     assert st(_params(head_dim=512), 0, FAKE, FAKE, FAKE) == G.G4_ERR_SHARE_MISMATCH
 
 
+def test_ring_cache_validation(L):
+    # Sliding-window ring caches: only on sliding layers, at least a window of
+    # rows, and a prefill chunk must leave every key of its windows resident.
+    W = 512
+    def ring(max_len, lt=G.G4_SLIDING, hd=256, dt=G.G4_BF16, flag=1):
+        t = _table([(lt, hd, 2, max_len, 1, dt)])
+        t[0].ring = flag   # the raw field, so that values other than 0 / 1 reach the library
+        return t
+
+    full = _params(layer_type=G.G4_FULL, head_dim=512, theta=1e6, rotary_fraction=0.25, window=0)
+
+    def pf(p, tab, T, B=1):   # B=0: every host check, no launch
+        return _status(G.g4_attn_prefill, p, tab, 0, FAKE, FAKE, B, T, FAKE, 0)
+
+    assert pf(_params(), ring(1024, flag=2), 4) == G.G4_ERR_INVALID_ARG
+    assert pf(full, ring(1024, lt=G.G4_FULL, hd=512), 4) == G.G4_ERR_INVALID_ARG
+    assert pf(_params(), ring(W - 1), 1) == G.G4_ERR_CAPACITY
+    # T + W - 1 keys: 513 + 511 = 1024 fit a 1024-row ring, 514 do not
+    assert pf(_params(), ring(1024), 514) == G.G4_ERR_CAPACITY
+    assert pf(_params(), ring(1024), 0) == G.G4_OK
+    # the bf16 prefill needs whole 128-key tiles in the ring; float32 does not
+    assert pf(_params(), ring(1000), 0) == G.G4_ERR_UNSUPPORTED
+    assert pf(_params(dtype=G.G4_F32), ring(1000, dt=G.G4_F32), 0) == G.G4_OK
+    # with a one-token window a chunk may fill the whole ring, not more
+    assert pf(_params(window=1), ring(256), 256, B=0) == G.G4_OK
+    assert pf(_params(window=1), ring(256), 257) == G.G4_ERR_CAPACITY
+
+    # decode: the sequence may be longer than the ring
+    def dec(tab, maxlen, B=0):
+        return _status(G.g4_attn_decode, _params(), tab, 0, FAKE, FAKE, B, maxlen, FAKE, FAKE, 1 << 30, 0)
+
+    assert dec(ring(W), 100000) == G.G4_OK
+    assert dec(ring(W, flag=0), 100000) == G.G4_ERR_CAPACITY
+    assert dec(ring(W - 1), 100) == G.G4_ERR_CAPACITY
+
+    # append: a ring is validated like any cache
+    def ap(tab):
+        return _status(G.g4_kv_append_normrope, _params(), tab, 0, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 2,
+                       FAKE, 0)
+
+    assert ap(ring(W)) == G.G4_OK
+    assert ap(ring(W - 1)) == G.G4_ERR_CAPACITY
+
+
 def test_tiny_config_literal_layer_types_are_rejected(L):
     # The tiny config's literal [S, S, S, F] with the last two layers shared
     # routes the full tail layer (head_dim 128) to layer 1, a sliding layer of
