@@ -35,6 +35,10 @@ What it computes, and where each step comes from (page title + function):
                         (turbospark-runtime ``gemma4`` decode: ``ring_capacity``
                         and ``active_ring`` passed to the attention next to
                         ``kv_start = seq_len - sliding_window``).
+* ``attention_bidirectional`` -- the encoder form of the same attention
+                        (taconite-embeddinggemma2 ``model.rs``:
+                        ``text_attention``): no causal mask, and a sliding
+                        layer sees the keys with |i - j| <= window.
 * ``kv_share_src``   -- shared-KV routing of the tail layers
                         (ferrox-models ``Gemma4Hparams::kv_reuse_layer``;
                         cortiq-engine ``g4e.rs`` module doc on shared KV).
@@ -368,6 +372,50 @@ def attention_rows(q, cache_k, cache_v, rows, q_pos, kv_len, n_kv_heads, layer_t
         p = attention_probs(q[b, t, h], K, j, int(q_pos[b, t]), layer_type, window, scale)
         res.append(p @ V)
     return np.stack(res) if res else np.zeros((0, q.shape[-1]))
+
+
+def visible_bidirectional(q_pos, k_pos, layer_type, window):
+    """Key at k_pos is visible from a query at q_pos in the encoder form:
+    every key on a global layer, |q - k| <= window on a sliding one
+    (taconite-embeddinggemma2 ``text_attention``: keys lo..hi-1 with
+    lo = i - win saturating at 0 and hi = min(i + win + 1, n); win is the
+    sliding window, or n where the window cuts nothing off)."""
+    q_pos = np.asarray(q_pos)
+    k_pos = np.asarray(k_pos)
+    vis = np.ones(np.broadcast(q_pos, k_pos).shape, dtype=bool)
+    if layer_type == SLIDING:
+        vis = np.abs(q_pos - k_pos) <= window
+    return vis
+
+
+def attention_bidirectional(q, cache_k, cache_v, T, n_kv_heads, layer_type, window, scale=1.0):
+    """Encoder attention over one sequence of T tokens per batch entry.
+
+    q [B, T, H, hd] (normed and roped at positions 0..T-1); the keys and
+    values of the same tokens in cache rows [0, T) of cache_k / cache_v
+    [B, Hkv, Lmax, hd].  o[b, i, h] = sum_j softmax_j(scale * q . k_j) v_j
+    over the keys ``visible_bidirectional`` admits; head h reads kv head
+    h // (H / Hkv).  Returns float64 [B, T, H, hd].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    B, Tq, H, hd = q.shape
+    assert Tq == T
+    g = H // n_kv_heads
+    out = np.zeros((B, T, H, hd), dtype=np.float64)
+    i = np.arange(T)
+    vis = visible_bidirectional(i[:, None], i[None, :], layer_type, window)   # [T, T]
+    for b in range(B):
+        for h in range(H):
+            kvh = h // g
+            K = np.asarray(cache_k[b, kvh, :T], dtype=np.float64)
+            V = np.asarray(cache_v[b, kvh, :T], dtype=np.float64)
+            S = (q[b, :, h, :] @ K.T) * scale
+            S = np.where(vis, S, -np.inf)
+            m = np.max(S, axis=1, keepdims=True)
+            P = np.exp(S - m)
+            P = P / np.sum(P, axis=1, keepdims=True)
+            out[b, :, h, :] = P @ V
+    return out
 
 
 # --------------------------------------------------------------------------

@@ -511,3 +511,93 @@ def test_ring_too_small_or_on_a_full_layer_is_refused():
         O.attention(q, ck2, ck2, pos, [10 + T], Hkv, O.FULL, W, ring=True)
     with pytest.raises(ValueError):
         O.ring_slot(-1, 4)
+
+
+# ------------------------------------------- bidirectional (encoder) attention
+
+@pytest.mark.parametrize("layer_type,window", [(O.FULL, 0), (O.SLIDING, 4), (O.SLIDING, 0), (O.SLIDING, 30)])
+def test_bidirectional_matches_torch_sdpa_band_mask(layer_type, window):
+    # library routine: torch SDPA in float64, no causal mask, the band
+    # |i - j| <= W as an explicit boolean mask on sliding layers
+    B, T, H, Hkv, hd = 2, 17, 4, 2, 32
+    r = rng(40 + window)
+    q = r.standard_normal((B, T, H, hd))
+    k = r.standard_normal((B, T, Hkv, hd))
+    v = r.standard_normal((B, T, Hkv, hd))
+    ck, cv = _cache_from(k, v, Lmax=T + 5)
+    ck[:, :, T:] = np.nan     # rows past T are never read
+    cv[:, :, T:] = np.nan
+    got = O.attention_bidirectional(q, ck, cv, T, Hkv, layer_type, window, 1.0)
+    i = torch.arange(T)[:, None]
+    j = torch.arange(T)[None, :]
+    mask = torch.ones(T, T, dtype=torch.bool)
+    if layer_type == O.SLIDING:
+        mask = (i - j).abs() <= window
+    qt = torch.from_numpy(q).permute(0, 2, 1, 3)
+    kt = torch.from_numpy(k).permute(0, 2, 1, 3).repeat_interleave(H // Hkv, dim=1)
+    vt = torch.from_numpy(v).permute(0, 2, 1, 3).repeat_interleave(H // Hkv, dim=1)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=1.0)
+    assert np.allclose(got, ref.permute(0, 2, 1, 3).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_bidirectional_brute_force_loops():
+    # explicit loops over the key interval [i - W, i + W] clipped to the sequence
+    B, T, H, Hkv, hd, W = 1, 9, 2, 1, 4, 2
+    r = rng(41)
+    q = r.standard_normal((B, T, H, hd))
+    k = r.standard_normal((B, T, Hkv, hd))
+    v = r.standard_normal((B, T, Hkv, hd))
+    ck, cv = _cache_from(k, v)
+    for lt in (O.FULL, O.SLIDING):
+        got = O.attention_bidirectional(q, ck, cv, T, Hkv, lt, W)
+        for t in range(T):
+            lo, hi = (max(0, t - W), min(T, t + W + 1)) if lt == O.SLIDING else (0, T)
+            for h in range(H):
+                js = list(range(lo, hi))
+                sc = [sum(q[0, t, h, d] * k[0, j, 0, d] for d in range(hd)) for j in js]
+                mx = max(sc)
+                ws = [math.exp(s - mx) for s in sc]
+                z = sum(ws)
+                exp = [sum(w * v[0, j, 0, d] for w, j in zip(ws, js)) / z for d in range(hd)]
+                assert np.allclose(got[0, t, h], exp, rtol=1e-12, atol=1e-13)
+
+
+def test_bidirectional_is_symmetric_under_reversal():
+    # The band is symmetric: reversing the tokens reverses the output.  A
+    # causal or one-sided mask fails this.
+    B, T, H, Hkv, hd, W = 2, 15, 2, 2, 16, 3
+    r = rng(42)
+    q = r.standard_normal((B, T, H, hd))
+    k = r.standard_normal((B, T, Hkv, hd))
+    v = r.standard_normal((B, T, Hkv, hd))
+    ck, cv = _cache_from(k, v)
+    rk, rv = _cache_from(k[:, ::-1], v[:, ::-1])
+    for lt in (O.FULL, O.SLIDING):
+        fwd = O.attention_bidirectional(q, ck, cv, T, Hkv, lt, W)
+        bwd = O.attention_bidirectional(q[:, ::-1], rk, rv, T, Hkv, lt, W)
+        assert np.allclose(bwd[:, ::-1], fwd, rtol=1e-12, atol=1e-12)
+
+
+def test_bidirectional_window_special_cases():
+    B, T, H, Hkv, hd = 1, 12, 4, 2, 16
+    r = rng(43)
+    q = r.standard_normal((B, T, H, hd))
+    k = r.standard_normal((B, T, Hkv, hd))
+    v = r.standard_normal((B, T, Hkv, hd))
+    ck, cv = _cache_from(k, v)
+    # W = 0: each token sees itself alone, o_i = v_i
+    o0 = O.attention_bidirectional(q, ck, cv, T, Hkv, O.SLIDING, 0)
+    for h in range(H):
+        assert np.allclose(o0[0, :, h], v[0, :, h // 2], rtol=0, atol=1e-15)
+    # a window reaching every key (W >= T - 1) is the global layer
+    full = O.attention_bidirectional(q, ck, cv, T, Hkv, O.FULL, 0)
+    assert np.array_equal(O.attention_bidirectional(q, ck, cv, T, Hkv, O.SLIDING, T - 1), full)
+    assert not np.allclose(O.attention_bidirectional(q, ck, cv, T, Hkv, O.SLIDING, T - 2), full)
+    # the last token sees [T-1-W, T-1]: the causal window of W + 1 keys
+    # (current included) at the same query -- the two conventions differ by one
+    W = 4
+    pos = np.arange(T)[None, :]
+    bi = O.attention_bidirectional(q, ck, cv, T, Hkv, O.SLIDING, W)
+    causal = O.attention(q, ck, cv, pos, [T], Hkv, O.SLIDING, W + 1)
+    assert np.allclose(bi[0, T - 1], causal[0, T - 1], rtol=0, atol=1e-14)
+    assert not np.allclose(bi[0, T - 1], O.attention(q, ck, cv, pos, [T], Hkv, O.SLIDING, W)[0, T - 1])
