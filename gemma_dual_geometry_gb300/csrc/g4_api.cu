@@ -255,6 +255,7 @@ g4_status g4_attn_prefill(const g4_layer_params* params, const g4_kv_cache* cach
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (params->dtype == G4_BF16) {
     g4::PrefillTcArgs a;
+    memset(&a, 0, sizeof(a));
     a.q = q;
     a.ck = c->k;
     a.cv = c->v;
@@ -296,6 +297,73 @@ g4_status g4_attn_prefill(const g4_layer_params* params, const g4_kv_cache* cach
   a.nsplit = 1;
   a.scale_log2 = scale_log2;
   return cuda_status(g4::launch_attn_simt(a, params->dtype, s), "float32 prefill launch");
+}
+
+g4_status g4_attn_encoder(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
+                          int32_t layer, const void* q, int32_t B, int32_t T, void* out, void* stream) {
+  g4_status st = check_params(params);
+  if (st != G4_OK) return st;
+  if (B < 0 || T < 0) return fail(G4_ERR_INVALID_ARG, "B %d and T %d must be >= 0", B, T);
+  if (q == nullptr || out == nullptr) return fail(G4_ERR_INVALID_ARG, "q and out must be non-NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(G4_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  const g4_kv_cache* c = nullptr;
+  st = resolve_src(params, caches, n_layers, layer, &c);
+  if (st != G4_OK) return st;
+  if (c->ring)
+    return fail(G4_ERR_INVALID_ARG, "the encoder reads the sequence's keys at rows 0 .. T-1: a ring cache cannot hold them");
+  if (c->batch < B) return fail(G4_ERR_CAPACITY, "cache batch %d < B %d", c->batch, B);
+  if (T > c->max_len) return fail(G4_ERR_CAPACITY, "T %d exceeds the cache length %d", T, c->max_len);
+  if (B == 0 || T == 0) return ok();
+  int* err = device_error_ptr();
+  if (err == nullptr) return fail(G4_ERR_CUDA, "cannot resolve the device error word");
+  const bool sliding = params->layer_type == G4_SLIDING;
+  // A window of T or more keys reaches every key; capping it keeps i + window
+  // in range.
+  const int window = sliding ? (params->window < T ? params->window : T) : 0;
+  const float scale_log2 = params->attn_scale * 1.4426950408889634f;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (params->dtype == G4_BF16) {
+    g4::PrefillTcArgs a;
+    memset(&a, 0, sizeof(a));
+    a.q = q;
+    a.ck = c->k;
+    a.cv = c->v;
+    a.out = out;
+    a.q_start = nullptr;  // unused: token t sits at position t
+    a.err = err;
+    a.B = B;
+    a.T = T;
+    a.H = params->n_heads;
+    a.Hkv = params->n_kv_heads;
+    a.hd = params->head_dim;
+    a.max_len = c->max_len;
+    a.sliding = sliding;
+    a.window = window;
+    a.bidir = 1;
+    a.scale_log2 = scale_log2;
+    return cuda_status(g4::launch_prefill_tc(a, s), "tcgen05 encoder launch");
+  }
+  g4::AttnSimtArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.ck = c->k;
+  a.cv = c->v;
+  a.out = out;
+  a.err = err;
+  a.mode = 2;
+  a.B = B;
+  a.T = T;
+  a.H = params->n_heads;
+  a.Hkv = params->n_kv_heads;
+  a.hd = params->head_dim;
+  a.max_len = c->max_len;
+  a.sliding = sliding;
+  a.window = window;
+  a.len_cap = c->max_len;
+  a.chunk = sliding ? 2 * window + 1 : T;  // one split holds a query's whole key range
+  a.nsplit = 1;
+  a.scale_log2 = scale_log2;
+  return cuda_status(g4::launch_attn_simt(a, params->dtype, s), "float32 encoder launch");
 }
 
 size_t g4_attn_decode_workspace_size(const g4_layer_params* params, int32_t B, int32_t max_seq_len) {

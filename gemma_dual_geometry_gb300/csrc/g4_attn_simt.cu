@@ -320,15 +320,22 @@ __global__ void __launch_bounds__(NW * 32, (SimtCfg<T, HD, G, NW>::MINB))
   pdl_trigger();
 
   // Query position and visible key range [kbeg, L).
-  int L;
-  if (a.mode == 0) {
-    L = min(max(a.base[b], 1), a.len_cap);
-  } else if (a.ring) {
-    L = max(a.base[b] + t, 0) + 1;  // every position has a row in a ring
+  int L, kbeg;
+  if (!FUSED && a.mode == 2) {
+    // encoder: token t of the sequence's T keys, no causal mask (the host
+    // caps the window at T)
+    kbeg = a.sliding ? max(0, t - a.window) : 0;
+    L = a.sliding ? min(a.T, t + a.window + 1) : a.T;
   } else {
-    L = min(max(a.base[b] + t, 0), a.max_len - 1) + 1;
+    if (a.mode == 0) {
+      L = min(max(a.base[b], 1), a.len_cap);
+    } else if (a.ring) {
+      L = max(a.base[b] + t, 0) + 1;  // every position has a row in a ring
+    } else {
+      L = min(max(a.base[b] + t, 0), a.max_len - 1) + 1;
+    }
+    kbeg = a.sliding ? max(0, L - a.window) : 0;
   }
-  const int kbeg = a.sliding ? max(0, L - a.window) : 0;
   const int k0 = kbeg + split * a.chunk;
   const int k1 = min(L, k0 + a.chunk);
   // FUSED: the CTA holding position L-1 computes that key itself.

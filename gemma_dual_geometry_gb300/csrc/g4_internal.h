@@ -33,7 +33,9 @@ cudaError_t launch_append(const AppendArgs& a, int dtype, cudaStream_t s);
 
 // Steps a5 (float32) and a6: split-KV softmax attention on CUDA cores.
 // mode 0 (decode): one query per sequence at position base[b] - 1, keys
-//   [kstart, base[b]); mode 1 (prefill): query t at position base[b] + t.
+//   [kstart, base[b]); mode 1 (prefill): query t at position base[b] + t;
+// mode 2 (encoder, not fused): query t of a sequence of T tokens whose keys
+//   are rows [0, T), keys [t - window, t + window] (sliding) or all T.
 // With fused set (decode only), q / k_raw / v_raw are the new token's raw
 // projections: each CTA norms and ropes its q heads, and the CTA whose split
 // holds position L-1 norms/ropes the new k and v, writes them to the cache
@@ -83,6 +85,8 @@ struct PrefillTcArgs {
   int B, T, H, Hkv, hd, max_len;
   int ring;          // 1: key position p is row p mod max_len (max_len a multiple of 128)
   int sliding, window;
+  int bidir;         // 1: encoder form -- rows [0, T) hold the sequence's keys, no causal
+                     //    mask, |i - j| <= window on sliding layers; q_start unused
   float scale_log2;
   unsigned* item_ctr;  // [2]: next work item, CTAs done (zero between launches; set by the launcher)
 };

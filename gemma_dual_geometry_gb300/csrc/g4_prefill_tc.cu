@@ -153,7 +153,7 @@ struct TcItem {
   int q0, valid_rows, qpos_first, Lk, kt_begin, ntiles;
 };
 
-template <int NDH>
+template <int NDH, bool BIDIR>
 __device__ __forceinline__ TcItem tc_item(const PrefillTcArgs& a, int it, int nqt) {
   TcItem w;
   const int grp = a.H / a.Hkv;
@@ -167,21 +167,30 @@ __device__ __forceinline__ TcItem tc_item(const PrefillTcArgs& a, int it, int nq
   w.kvh = idx % a.Hkv;
   w.b = idx / a.Hkv;
   w.h = w.kvh * grp + hq;
-  const int q_start = a.q_start[w.b];
+  const int q_start = BIDIR ? 0 : a.q_start[w.b];
   w.q0 = qt * kBM;
   w.valid_rows = min(kBM, a.T - w.q0);
   w.qpos_first = q_start + w.q0;
   const int qpos_last = w.qpos_first + w.valid_rows - 1;
-  // keys held: positions [0, Lk) (a ring holds the last max_len of them)
-  w.Lk = a.ring ? q_start + a.T : min(q_start + a.T, a.max_len);
-  const int kend = min(qpos_last + 1, w.Lk);
-  const int kbeg = a.sliding ? max(0, w.qpos_first - a.window + 1) : 0;
+  int kbeg, kend;
+  if constexpr (BIDIR) {
+    // Encoder: the sequence's own T keys, no causal mask; query i sees
+    // [i - window, i + window] on a sliding layer (window <= T here).
+    w.Lk = a.T;
+    kbeg = a.sliding ? max(0, w.qpos_first - a.window) : 0;
+    kend = a.sliding ? min(qpos_last + a.window + 1, w.Lk) : w.Lk;
+  } else {
+    // keys held: positions [0, Lk) (a ring holds the last max_len of them)
+    w.Lk = a.ring ? q_start + a.T : min(q_start + a.T, a.max_len);
+    kend = min(qpos_last + 1, w.Lk);
+    kbeg = a.sliding ? max(0, w.qpos_first - a.window + 1) : 0;
+  }
   w.kt_begin = kbeg / kBN;
   w.ntiles = max(0, (kend + kBN - 1) / kBN - w.kt_begin);
   return w;
 }
 
-template <int HD>
+template <int HD, bool BIDIR>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -283,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<volatile int*>(&bars->items[e]) = it;
         mbar_arrive(smem_u32(&bars->it_full[e]));
         if (it < 0) break;
-        const TcItem w = tc_item<C::NDH>(a, it, nqt);
+        const TcItem w = tc_item<C::NDH, BIDIR>(a, it, nqt);
         if (w.ntiles == 0) continue;
         if (nq > 0 && !thread_wait(smem_u32(&bars->q_free), (nq - 1) & 1, a.err, abort)) break;
         mbar_arrive_expect_tx(qb, C::QCH * kChunkB);
@@ -374,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int it = *reinterpret_cast<volatile int*>(&bars->items[e]);
         mbar_arrive(smem_u32(&bars->it_empty[e]));
         if (it < 0) break;
-        const TcItem w = tc_item<C::NDH>(a, it, nqt);
+        const TcItem w = tc_item<C::NDH, BIDIR>(a, it, nqt);
         if (w.ntiles == 0) continue;
         if (!thread_wait(smem_u32(&bars->q_full), nq & 1, a.err, abort)) break;
         ++nq;
@@ -481,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         softmax_sync_any(1);
         break;
       }
-      const TcItem w = tc_item<C::NDH>(a, it, nqt);
+      const TcItem w = tc_item<C::NDH, BIDIR>(a, it, nqt);
       const int ntiles = w.ntiles;
       if (ntiles == 0) {
         // No visible key (only reachable with out-of-contract positions).
@@ -526,8 +535,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             s[32 + i] = __uint_as_float(r1[i]);
           }
           const int kr = (w.kt_begin + j) * kBN;
-          const bool row_vis = row_valid && (kr + kBN - 1 <= qpos) && (kr + kBN <= w.Lk) &&
-                               (!a.sliding || qpos - kr < a.window);
+          const bool row_vis =
+              BIDIR ? row_valid && (kr + kBN <= w.Lk) &&
+                          (!a.sliding || (qpos - kr <= a.window && kr + kBN - 1 - qpos <= a.window))
+                    : row_valid && (kr + kBN - 1 <= qpos) && (kr + kBN <= w.Lk) &&
+                          (!a.sliding || qpos - kr < a.window);
           const int k0 = kr + half * kHB;
           const int k1 = kr + (1 - half) * kHB;
           float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -539,9 +551,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
             // The row's visible keys are one interval [vlo, vhi): causal end,
-            // the cache's filled length and (sliding) the window start.
-            const int vlo = a.sliding ? max(0, qpos - a.window + 1) : 0;
-            const int vhi = row_valid ? min(qpos + 1, w.Lk) : 0;
+            // the cache's filled length and (sliding) the window start; in
+            // the encoder form the window's two ends and the sequence end.
+            const int vlo = a.sliding ? max(0, qpos - a.window + (BIDIR ? 0 : 1)) : 0;
+            const int vhi = !row_valid ? 0
+                            : BIDIR    ? (a.sliding ? min(qpos + a.window + 1, w.Lk) : w.Lk)
+                                       : min(qpos + 1, w.Lk);
             const unsigned span = static_cast<unsigned>(max(0, vhi - vlo));
             const int lo0 = vlo - k0, lo1 = vlo - k1;
 #pragma unroll
@@ -720,13 +735,13 @@ bool make_map(CUtensorMap* m, const void* base, const cuuint64_t dims[5], const 
   return r == CUDA_SUCCESS;
 }
 
-template <int HD>
+template <int HD, bool BIDIR>
 cudaError_t launch_hd(const PrefillTcArgs& a, cudaStream_t s) {
   using C = TcCfg<HD>;
   static bool attr_set = false;
   if (!attr_set) {
     const cudaError_t e =
-        cudaFuncSetAttribute(prefill_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_B);
+        cudaFuncSetAttribute(prefill_tc_kernel<HD, BIDIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_B);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -775,7 +790,7 @@ cudaError_t launch_hd(const PrefillTcArgs& a, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD>, mq, mk, mv, mo, a);
+  return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<HD, BIDIR>, mq, mk, mv, mo, a);
 }
 
 }  // namespace
@@ -804,11 +819,20 @@ cudaError_t launch_prefill_tc(const PrefillTcArgs& a_in, cudaStream_t s) {
     }
     a.item_ctr = base[dev] + 2 * (next_slot++ % kCtrSlots);
   }
+  if (a.bidir) {
+    switch (a.hd) {
+      case 64: return launch_hd<64, true>(a, s);
+      case 128: return launch_hd<128, true>(a, s);
+      case 256: return launch_hd<256, true>(a, s);
+      case 512: return launch_hd<512, true>(a, s);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (a.hd) {
-    case 64: return launch_hd<64>(a, s);
-    case 128: return launch_hd<128>(a, s);
-    case 256: return launch_hd<256>(a, s);
-    case 512: return launch_hd<512>(a, s);
+    case 64: return launch_hd<64, false>(a, s);
+    case 128: return launch_hd<128, false>(a, s);
+    case 256: return launch_hd<256, false>(a, s);
+    case 512: return launch_hd<512, false>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -49,6 +49,8 @@ SIGNATURES = {
                                      _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _c_void_p]),
     "g4_attn_prefill": (_i32, [_P(G4LayerParams), _P(G4KVCache), _i32, _i32, _c_void_p, _c_void_p, _i32, _i32,
                                _c_void_p, _c_void_p]),
+    "g4_attn_encoder": (_i32, [_P(G4LayerParams), _P(G4KVCache), _i32, _i32, _c_void_p, _i32, _i32, _c_void_p,
+                               _c_void_p]),
     "g4_attn_decode_workspace_size": (ctypes.c_size_t, [_P(G4LayerParams), _i32, _i32]),
     "g4_attn_decode": (_i32, [_P(G4LayerParams), _P(G4KVCache), _i32, _i32, _c_void_p, _c_void_p, _i32, _i32,
                               _c_void_p, _c_void_p, ctypes.c_size_t, _c_void_p]),
@@ -140,6 +142,11 @@ def g4_kv_append_normrope(params, caches, layer, q_in, k_in, v_in, q_norm_w, k_n
 def g4_attn_prefill(params, caches, layer, q, q_start_pos, B, T, out, stream=None):
     _check(lib().g4_attn_prefill(ctypes.byref(params), caches, len(caches), layer, _ptr(q), _ptr(q_start_pos), B, T,
                                  _ptr(out), _stream(stream, q)))
+
+
+def g4_attn_encoder(params, caches, layer, q, B, T, out, stream=None):
+    _check(lib().g4_attn_encoder(ctypes.byref(params), caches, len(caches), layer, _ptr(q), B, T, _ptr(out),
+                                 _stream(stream, q)))
 
 
 def g4_attn_decode_workspace_size(params, B, max_seq_len):

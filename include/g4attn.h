@@ -9,7 +9,7 @@
  *   2. g4_attn_prefill / g4_attn_decode: causal GQA softmax attention with
  *      score scale attn_scale (1.0 for Gemma-4), windowed on sliding layers,
  *      over the cache of the layer itself or, on a shared-KV tail layer, of
- *      its source layer.
+ *      its source layer.  g4_attn_encoder: the bidirectional (encoder) form.
  *
  * Sources (page title + item):
  *   cortiq-engine g4e.rs: `rms`, `rms_plain`, `G4eGlobals` (inv_freq tables,
@@ -193,6 +193,24 @@ g4_status g4_kv_append_normrope(const g4_layer_params* params, const g4_kv_cache
 g4_status g4_attn_prefill(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
                           int32_t layer, const void* q, const int32_t* q_start_pos, int32_t B, int32_t T,
                           void* out, void* stream);
+
+/*
+ * Bidirectional (encoder) attention, the form of taconite-embeddinggemma2
+ * model.rs `text_attention`: no causal mask; a key j is visible from query i
+ * iff |i - j| <= window on a sliding layer (the window counts keys on each
+ * side, the token itself in the middle), every key on a full layer.
+ *   q    [B][T][n_heads][head_dim], normed + roped at positions 0 .. T-1
+ *        (g4_kv_append_normrope's q_out with positions[b][t] = t)
+ *   out  [B][T][n_heads][head_dim]
+ * The keys and values are the same T tokens, rows [0, T) of caches[src]
+ * (appended by g4_kv_append_normrope at positions 0 .. T-1; src as in
+ * g4_attn_prefill).  A ring cache is refused (G4_ERR_INVALID_ARG); T must
+ * not exceed max_len (G4_ERR_CAPACITY).  Score scale attn_scale.  bf16 runs
+ * on the tcgen05 tensor cores, f32 on CUDA cores, like g4_attn_prefill (the
+ * bf16 kernel takes one of the same 64 work-item counter pairs).
+ */
+g4_status g4_attn_encoder(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
+                          int32_t layer, const void* q, int32_t B, int32_t T, void* out, void* stream);
 
 /*
  * Workspace bytes g4_attn_decode / g4_decode_step need for this layer, batch

@@ -222,6 +222,27 @@ def test_ring_cache_validation(L):
     assert ap(ring(W - 1)) == G.G4_ERR_CAPACITY
 
 
+def test_encoder_validation(L):
+    tab = _table([(G.G4_SLIDING, 256, 2, 100, 2, G.G4_BF16)])
+
+    def enc(p=None, tab=tab, B=2, T=4, q=FAKE, out=FAKE):
+        return _status(G.g4_attn_encoder, p or _params(), tab, 0, q, B, T, out, 0)
+
+    assert enc(B=0) == G.G4_OK
+    assert enc(T=0) == G.G4_OK
+    assert enc(B=3) == G.G4_ERR_CAPACITY
+    assert enc(T=101, B=0) == G.G4_ERR_CAPACITY
+    assert enc(T=-1) == G.G4_ERR_INVALID_ARG
+    assert enc(q=None) == G.G4_ERR_INVALID_ARG
+    assert enc(out=FAKE + 8) == G.G4_ERR_INVALID_ARG
+    assert enc(_params(head_dim=512)) == G.G4_ERR_SHARE_MISMATCH
+    assert enc(_params(window=0)) == G.G4_ERR_INVALID_ARG
+    # the encoder reads rows 0 .. T-1: no ring
+    ring = _table([(G.G4_SLIDING, 256, 2, 1024, 2, G.G4_BF16, True)])
+    assert enc(tab=ring, B=0) == G.G4_ERR_INVALID_ARG
+    assert "ring" in G.g4_last_error()
+
+
 def test_tiny_config_literal_layer_types_are_rejected(L):
     # The tiny config's literal [S, S, S, F] with the last two layers shared
     # routes the full tail layer (head_dim 128) to layer 1, a sliding layer of
