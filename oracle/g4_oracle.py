@@ -39,6 +39,16 @@ What it computes, and where each step comes from (page title + function):
                         (taconite-embeddinggemma2 ``model.rs``:
                         ``text_attention``): no causal mask, and a sliding
                         layer sees the keys with |i - j| <= window.
+* ``qkv_projection`` -- the step before the path: the layer input's RMSNorm
+                        (attn_norm) and the q / k / v projections
+                        (cortiq-engine ``g4e_forward``: ``rms(h, attn_norm)``
+                        then ``matvec`` with wq / wk / wv; memra-engine
+                        ``forward.rs``: ``rms_norm`` then the linear layers).
+* ``attn_output_residual`` -- the step after it: o_proj, the
+                        post-attention RMSNorm and the residual add
+                        (cortiq-engine ``g4e_forward`` "sandwich"; ferrox-models
+                        ``forward_token_on_worker``: ``o_proj``,
+                        ``post_attn_norm``, add to ``hidden``).
 * ``kv_share_src``   -- shared-KV routing of the tail layers
                         (ferrox-models ``Gemma4Hparams::kv_reuse_layer``;
                         cortiq-engine ``g4e.rs`` module doc on shared KV).
@@ -416,6 +426,34 @@ def attention_bidirectional(q, cache_k, cache_v, T, n_kv_heads, layer_type, wind
             P = P / np.sum(P, axis=1, keepdims=True)
             out[b, :, h, :] = P @ V
     return out
+
+
+# --------------------------------------------------------------------------
+# Before and after the path: projections, post-attention norm, residual
+# --------------------------------------------------------------------------
+
+def qkv_projection(x, attn_norm_w, wq, wk, wv, eps):
+    """Raw q / k / v of one layer from its input hidden state.
+
+    x [..., D]; attn_norm_w [D]; wq [H*hd, D]; wk, wv [Hkv*hd, D] (None on a
+    shared-KV layer, which projects q only).  xn = rms_norm(x, attn_norm_w)
+    and q = wq xn, k = wk xn, v = wv xn (a row of W per output, as the pages'
+    ``matvec`` / ``linear`` take it).  Returns (q, k, v), k and v None on a
+    shared layer; the caller splits the last axis into heads.
+    """
+    xn = rms_norm(x, attn_norm_w, eps)
+    q = xn @ np.asarray(wq, dtype=np.float64).T
+    k = None if wk is None else xn @ np.asarray(wk, dtype=np.float64).T
+    v = None if wv is None else xn @ np.asarray(wv, dtype=np.float64).T
+    return q, k, v
+
+
+def attn_output_residual(h, ao, wo, post_norm_w, eps):
+    """h + rms_norm(wo ao, post_norm_w): the attention output [..., H*hd]
+    projected back to the model width by wo [D, H*hd], normed with the
+    post-attention weight [D] and added to the residual stream h [..., D]."""
+    a = np.asarray(ao, dtype=np.float64) @ np.asarray(wo, dtype=np.float64).T
+    return np.asarray(h, dtype=np.float64) + rms_norm(a, post_norm_w, eps)
 
 
 # --------------------------------------------------------------------------

@@ -601,3 +601,58 @@ def test_bidirectional_window_special_cases():
     causal = O.attention(q, ck, cv, pos, [T], Hkv, O.SLIDING, W + 1)
     assert np.allclose(bi[0, T - 1], causal[0, T - 1], rtol=0, atol=1e-14)
     assert not np.allclose(bi[0, T - 1], O.attention(q, ck, cv, pos, [T], Hkv, O.SLIDING, W)[0, T - 1])
+
+
+# --------------------------------- before / after the path: projections, residual
+
+def test_qkv_projection_matches_torch_library():
+    # library routines: torch rms_norm and linear in float64
+    T, D, H, Hkv, hd = 5, 96, 4, 2, 16
+    r = rng(50)
+    x = r.standard_normal((T, D))
+    nw = 1 + 0.1 * r.standard_normal(D)
+    wq = r.standard_normal((H * hd, D)) / math.sqrt(D)
+    wk = r.standard_normal((Hkv * hd, D)) / math.sqrt(D)
+    wv = r.standard_normal((Hkv * hd, D)) / math.sqrt(D)
+    q, k, v = O.qkv_projection(x, nw, wq, wk, wv, 1e-6)
+    xt = torch.nn.functional.rms_norm(torch.from_numpy(x), (D,), torch.from_numpy(nw), 1e-6)
+    for got, w in ((q, wq), (k, wk), (v, wv)):
+        ref = torch.nn.functional.linear(xt, torch.from_numpy(w)).numpy()
+        assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+    # a shared layer projects q only
+    q2, k2, v2 = O.qkv_projection(x, nw, wq, None, None, 1e-6)
+    assert k2 is None and v2 is None and np.array_equal(q2, q)
+
+
+def test_qkv_projection_selection_matrix_is_the_normed_input():
+    # W = [I 0] picks the first outputs of the normed input exactly
+    D, n = 40, 24
+    r = rng(51)
+    x = r.standard_normal((3, D))
+    nw = 1 + 0.1 * r.standard_normal(D)
+    sel = np.zeros((n, D))
+    sel[np.arange(n), np.arange(n)] = 1.0
+    q, _, _ = O.qkv_projection(x, nw, sel, None, None, 1e-6)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    assert np.allclose(q, (x / np.sqrt(ms + 1e-6) * nw)[:, :n], rtol=1e-14, atol=0)
+
+
+def test_attn_output_residual_library_and_special_cases():
+    T, D, HD = 4, 64, 48
+    r = rng(52)
+    h = r.standard_normal((T, D))
+    ao = r.standard_normal((T, HD))
+    wo = r.standard_normal((D, HD)) / math.sqrt(HD)
+    pw = 1 + 0.1 * r.standard_normal(D)
+    got = O.attn_output_residual(h, ao, wo, pw, 1e-6)
+    a = torch.nn.functional.linear(torch.from_numpy(ao), torch.from_numpy(wo))
+    ref = torch.from_numpy(h) + torch.nn.functional.rms_norm(a, (D,), torch.from_numpy(pw), 1e-6)
+    assert np.allclose(got, ref.numpy(), rtol=1e-12, atol=1e-12)
+    # a zero projection adds nothing (0 * (0 + eps)^-1/2 = 0)
+    assert np.array_equal(O.attn_output_residual(h, ao, np.zeros_like(wo), pw, 1e-6), h)
+    # with eps = 0 the added term ignores the scale of the attention output,
+    # and with unit weight its mean square is 1
+    g1 = O.attn_output_residual(h, ao, wo, np.ones(D), 0.0)
+    g2 = O.attn_output_residual(h, 7.5 * ao, wo, np.ones(D), 0.0)
+    assert np.allclose(g1, g2, rtol=0, atol=1e-12)
+    assert np.allclose(np.mean((g1 - h) ** 2, axis=-1), 1.0, rtol=1e-12)
