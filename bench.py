@@ -170,10 +170,21 @@ def visible_pairs(T, window, sliding, q_start=0):
     return tot
 
 
+def visible_pairs_bidirectional(T, window, sliding):
+    """Sum over the T queries of the keys each one sees in the encoder form
+    (|i - j| <= window on a sliding layer, all T otherwise)."""
+    if not sliding:
+        return T * T
+    return sum(min(T, i + window + 1) - max(0, i - window) for i in range(T))
+
+
 def prefill_flops(cfg, layer):
     from gemma_dual_geometry_gb300 import workloads as W
     g = W.layer_geometry(cfg, layer)
-    pairs = visible_pairs(cfg["T"], g["window"], g["layer_type"] == W.SLIDING)
+    if cfg.get("encoder"):
+        pairs = visible_pairs_bidirectional(cfg["T"], g["window"], g["layer_type"] == W.SLIDING)
+    else:
+        pairs = visible_pairs(cfg["T"], g["window"], g["layer_type"] == W.SLIDING)
     return 4.0 * g["head_dim"] * cfg["H"] * cfg["B"] * pairs  # QK^T and PV, 2 flops per MAC
 
 
@@ -469,9 +480,10 @@ def run_ours(args, cfg):
 
 
 class LayerJob:
-    """One- or two-layer workloads: single-layer prefill (prefill_bf16) or
-    decode against prefilled caches (decode_bf16, longctx_decode_bf16).  A step
-    is append + attention for every layer of the workload."""
+    """One- or two-layer workloads: single-layer prefill (prefill_bf16), the
+    encoder form (encoder_bf16), or decode against prefilled caches
+    (decode_bf16, ring_decode_bf16, longctx_decode_bf16).  A step is append +
+    attention for every layer of the workload."""
 
     def __init__(self, cfg, device):
         import torch
@@ -482,6 +494,7 @@ class LayerJob:
         self.cfg, self.W, self.torch = cfg, W, torch
         self.B = cfg["B"]
         self.decode = "T" not in cfg
+        self.encoder = bool(cfg.get("encoder"))
         H, Hkv, dt = cfg["H"], cfg["Hkv"], cfg["dtype"]
         if self.decode:
             if "L" in cfg:
@@ -497,7 +510,7 @@ class LayerJob:
         self.n = self.st.n
         if self.decode:
             for l in range(self.n):
-                k, v = W.prefilled_cache(cfg, l, self.Lmax, device=device)
+                k, v = W.prefilled_cache(cfg, l, W.cache_rows(cfg, l, self.Lmax), device=device)
                 self.st.caches[l][0].copy_(k)
                 self.st.caches[l][1].copy_(v)
                 del k, v
@@ -533,6 +546,8 @@ class LayerJob:
                 self.st.decode_step(l, x["q"].view(self.B, H, hd), x["k"].view(self.B, Hkv, hd),
                                     x["v"].view(self.B, Hkv, hd), x["q_norm_w"], x["k_norm_w"], self.sl, self.Lmax,
                                     self.out[l].view(self.B, H, hd))
+            elif self.encoder:
+                self.st.encoder_attn(l, self.qo[l], self.T, self.out[l])
             else:
                 self.st.prefill_attn(l, self.qo[l], self.qs, self.T, self.out[l])
             if ev is not None:
@@ -596,9 +611,11 @@ def run_layers(args, cfg):
         step_bytes = sum(job.layer_work(l) for l in range(job.n))
         value, unit = step_bytes * args.steps * world / total / 1e9, "GB/s"
         what = f"B={job.B} decode, lengths {min(job.L)}..{max(job.L)}"
+        if cfg.get("ring"):
+            what += ", sliding cache a ring of one window"
     else:
         value, unit = job.B * job.T * args.steps * world / total, "tokens/s"
-        what = f"B={job.B} prefill, T={job.T}"
+        what = f"B={job.B} {'encoder (bidirectional)' if job.encoder else 'prefill'}, T={job.T}"
     line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1), on device)",

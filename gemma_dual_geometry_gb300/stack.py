@@ -2,7 +2,8 @@
 
 Owns the device buffers of a stack (one KV cache per layer that owns one,
 q_out scratch per head width, decode workspaces) and sequences the per-layer
-calls: g4_kv_append_normrope then g4_attn_prefill / g4_attn_decode.  Shared-KV
+calls: g4_kv_append_normrope then g4_attn_prefill / g4_attn_decode (or
+g4_attn_encoder).  Sliding caches may be rings of one window.  Shared-KV
 tail layers get no cache and read their source layer's
 (cortiq-engine g4e.rs `g4e_forward`: `src = kv_share_src.unwrap_or(li)`).
 Every step runs in the CUDA kernels; this module only allocates and calls.
@@ -36,12 +37,14 @@ class AttnStack:
         tdt = W.torch_dtype(cfg["dtype"])
         for l, g in enumerate(self.geo):
             if self.src[l] < 0:
-                shape = (self.B, cfg["Hkv"], Lmax, g["head_dim"])
+                # a ring (sliding layers of a ring workload) holds one window
+                rows = W.cache_rows(cfg, l, Lmax)
+                shape = (self.B, cfg["Hkv"], rows, g["head_dim"])
                 k = torch.zeros(shape, dtype=tdt, device=self.device)
                 v = torch.zeros(shape, dtype=tdt, device=self.device)
                 self.caches[l] = (k, v)
-                G.set_cache(self.table, l, k, v, g["layer_type"], g["head_dim"], cfg["Hkv"], Lmax, self.B,
-                            cfg["dtype"])
+                G.set_cache(self.table, l, k, v, g["layer_type"], g["head_dim"], cfg["Hkv"], rows, self.B,
+                            cfg["dtype"], ring=bool(cfg.get("ring")) and g["layer_type"] == W.SLIDING)
         self.ws = {}
         for l, p in enumerate(self.params):
             nb = G.g4_attn_decode_workspace_size(p, self.B, Lmax)
@@ -59,6 +62,10 @@ class AttnStack:
 
     def prefill_attn(self, l, q_out, q_start, T, out, stream=None):
         G.g4_attn_prefill(self.params[l], self.table, l, q_out, q_start, self.B, T, out, stream=stream)
+
+    def encoder_attn(self, l, q_out, T, out, stream=None):
+        """Bidirectional attention over the T tokens appended at positions 0..T-1."""
+        G.g4_attn_encoder(self.params[l], self.table, l, q_out, self.B, T, out, stream=stream)
 
     def decode_attn(self, l, q_out, seq_lens, max_seq_len, out, stream=None):
         ws, nb = self.ws[l]

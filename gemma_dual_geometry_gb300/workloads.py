@@ -59,6 +59,18 @@ CONFIGS = {
         B=8, T=4096, decode_steps=8, H=8, Hkv=2, dtype=BF16, seed=3,
         types=[FULL if (i + 1) % 6 == 0 else SLIDING for i in range(42)], n_shared=18,
         geom={SLIDING: SLIDING_GEOM_BF16, FULL: FULL_GEOM_BF16}),
+    # decode_bf16 with the sliding layer's cache as a ring of one window
+    # (512 rows instead of the longest length): same keys read per step
+    "ring_decode_bf16": dict(
+        B=64, L_lo=1024, L_hi=8192, H=8, Hkv=2, dtype=BF16, seed=2, ring=True,
+        types=[SLIDING, FULL], n_shared=0,
+        geom={SLIDING: SLIDING_GEOM_BF16, FULL: FULL_GEOM_BF16}),
+    # bidirectional (encoder) attention over T tokens, both layer types; the
+    # encoder page ropes every pair on both (rotary fraction 1.0)
+    "encoder_bf16": dict(
+        B=4, T=2048, H=8, Hkv=2, dtype=BF16, seed=5, encoder=True,
+        types=[SLIDING, FULL], n_shared=0,
+        geom={SLIDING: SLIDING_GEOM_BF16, FULL: dict(FULL_GEOM_BF16, rotary_fraction=1.0)}),
     "longctx_decode_bf16": dict(
         B=4, L=131072, H=8, Hkv=2, dtype=BF16, seed=4,
         types=[FULL, SLIDING], n_shared=0,
@@ -126,6 +138,15 @@ def layer_inputs(cfg, layer, T, owns_cache, device="cpu", step=0, B=None):
         out["v"] = normal((B, T, Hkv, hd), seed_for(s, layer, 2, step), dt, device)
         out["k_norm_w"] = norm_weight(hd, seed_for(s, layer, 4))
     return out
+
+
+def cache_rows(cfg, layer, Lmax):
+    """Rows of a layer's cache: Lmax, or one window for a sliding layer of a
+    workload whose sliding caches are rings."""
+    geo = layer_geometry(cfg, layer)
+    if cfg.get("ring") and geo["layer_type"] == SLIDING:
+        return geo["window"]
+    return Lmax
 
 
 def prefilled_cache(cfg, layer, Lmax, device="cpu", B=None):

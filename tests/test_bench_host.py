@@ -35,6 +35,37 @@ def test_stack_workload_arithmetic():
     assert step == pytest.approx(1.248e9, rel=5e-3)
 
 
+def test_bidirectional_pairs_closed_forms():
+    # every key on a global layer; on a sliding one 2W+1 keys per query less
+    # W(W+1)/2 cut off at each end of the sequence (T >= W)
+    assert bench.visible_pairs_bidirectional(2048, 0, False) == 2048 * 2048
+    for T, Wn in ((2048, 512), (1000, 100), (300, 1), (7, 7)):
+        assert bench.visible_pairs_bidirectional(T, Wn, True) == T * (2 * Wn + 1) - Wn * (Wn + 1)
+    assert bench.visible_pairs_bidirectional(10, 0, True) == 10
+    cfg = W.CONFIGS["encoder_bf16"]
+    assert bench.prefill_flops(cfg, 0) == 4.0 * 256 * 8 * 4 * (2048 * 1025 - 512 * 513)
+    assert bench.prefill_flops(cfg, 1) == 4.0 * 512 * 8 * 4 * 2048 * 2048
+
+
+def test_ring_workload_builds_ring_caches_on_the_host():
+    # the stack driver's tables, built on CPU tensors (no kernel runs): the
+    # sliding layer's cache is a 512-row ring, the full layer's a linear cache
+    from gemma_dual_geometry_gb300 import build as g4build
+    from gemma_dual_geometry_gb300.stack import AttnStack
+    g4build.build()
+    cfg = dict(W.CONFIGS["ring_decode_bf16"], B=2)
+    st = AttnStack(cfg, 8192, device="cpu")
+    assert (st.table[0].ring, st.table[0].max_len) == (1, 512)
+    assert (st.table[1].ring, st.table[1].max_len) == (0, 8192)
+    assert st.caches[0][0].shape == (2, 2, 512, 256)
+    assert st.caches[1][0].shape == (2, 2, 8192, 512)
+    plain = AttnStack(dict(W.CONFIGS["decode_bf16"], B=2), 8192, device="cpu")
+    assert (plain.table[0].ring, plain.table[0].max_len) == (0, 8192)
+    # the decode bytes of a ring step are those of the linear cache
+    assert all(bench.decode_bytes(cfg, l, L) == bench.decode_bytes(dict(W.CONFIGS["decode_bf16"], B=2), l, L)
+               for l in (0, 1) for L in (1, 600, 8000))
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
