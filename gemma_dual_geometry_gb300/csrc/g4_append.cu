@@ -7,7 +7,8 @@
 // gemma4_engine.rs `forward_token_on_worker` does the same per head
 // (`rms_norm_per_head`, `apply_rope`, `cache.push`).  turbospark-runtime
 // gemma4/attn.rs writes the projections straight into the cache slot and
-// norms/ropes them there, which is the fusion done here.
+// norms/ropes them there, which is the fusion done here.  A token at
+// position p goes to cache row p, or p mod max_len on a sliding-window ring.
 //
 // One CTA (4 warps) handles the tokens at one t of up to tok_per_cta
 // consecutive sequences, rows_per_cta of each token's H + 2*Hkv head rows;

@@ -7,6 +7,11 @@
 // query head h reads kv head h / G (G = H / Hkv, contiguous groups as in
 // taconite `text_attention`), keys [kstart, L) with kstart = L - window on
 // sliding layers and 0 on full layers, scores scaled by attn_scale (1.0).
+// On a sliding-window ring cache (turbospark-runtime gemma4 decode:
+// `ring_capacity`) key position p is row p mod max_len, and a stage whose
+// keys cross the ring's last row is two copies.  Mode 2 (float32 encoder,
+// taconite-embeddinggemma2 `text_attention`): query t of a sequence sees its
+// keys [t - window, t + window] (sliding) or all T, with no causal mask.
 //
 // Work decomposition: one CTA per (split, kv head, query row).  All G query
 // heads of the kv head share every K/V row the CTA streams, so each key row

@@ -6,6 +6,14 @@
 // over keys j <= i (and i - j < window on sliding layers), query head h
 // reading kv head h / (H / Hkv).
 //
+// The BIDIR instantiation is the encoder form (taconite-embeddinggemma2
+// model.rs `text_attention`): the T tokens of a sequence are both queries
+// and keys (cache rows 0..T-1), with no causal mask, and key j is visible
+// from query i iff |i - j| <= window on a sliding layer.  Only the tile
+// range of a work item and the visible interval of a row differ.  On a
+// sliding-window ring cache (max_len rows, a multiple of the 128-key tile)
+// key position p is row p mod max_len; the masks stay in positions.
+//
 // A work item is a 128-query-row tile of one (sequence, head) and, for
 // head_dim 512, one 256-wide half of the output columns (two items per tile
 // then recompute the same scores; TMEM holds 512 f32 columns per SM and a
