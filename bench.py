@@ -45,7 +45,34 @@ DECODE_EVENT_STEPS = (0, 32, 64, 96, 127)
 # DRAM bytes (read + write) per launch from one ncu capture of each kernel on
 # the 42-layer stack with an 8-step decode phase (dram__bytes.sum.per_second x
 # gpu__time_duration); the decode figures are for the first decode step.
-PROFILED_TRAFFIC = {"prefill_full": 637334783, "decode_full": 137716979, "decode_sliding": 8492032}
+# Each figure carries the kernel's source files and the first 16 hex digits
+# of their SHA-256 when it was captured: once the sources differ, the
+# counters describe another kernel and the figure is not reported.
+PREFILL_SOURCES = ("g4_prefill_tc.cu", "g4_device.cuh", "g4_internal.h")
+DECODE_SOURCES = ("g4_attn_simt.cu", "g4_device.cuh", "g4_internal.h", "g4_normrope.cuh")
+PROFILED_TRAFFIC = {
+    "prefill_full": (637334783, PREFILL_SOURCES, "d1613f02eca7b99f"),
+    "decode_full": (137716979, DECODE_SOURCES, "dfacc6f82f285597"),
+    "decode_sliding": (8492032, DECODE_SOURCES, "dfacc6f82f285597"),
+}
+
+
+def kernel_sources_hash(files):
+    """First 16 hex digits of the SHA-256 of the concatenated kernel sources."""
+    import hashlib
+    m = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, "gemma_dual_geometry_gb300", "csrc", f), "rb") as fh:
+            m.update(fh.read())
+    return m.hexdigest()[:16]
+
+
+def profiled_traffic(key, source):
+    """(traffic per launch or None, where it comes from)."""
+    nbytes, files, digest = PROFILED_TRAFFIC[key]
+    if kernel_sources_hash(files) != digest:
+        return None, source + "; not reported: the kernel's sources changed after that capture"
+    return nbytes, source
 
 
 def parse_args(argv=None):
@@ -417,8 +444,9 @@ def run_ours(args, cfg):
                       achieved=pf_flops / pf_avg / 1e12, peak=peaks["bf16_tflops_sustained"], unit="TFLOP/s",
                       peak_kind=f"{peak_src} bf16 dense, sustained (timed inside a long step)",
                       flops_per_launch=pf_flops, avg_launch_ms=pf_avg * 1e3, launches_sampled=len(pf_launch),
-                      launches_per_step=len(job.full_layers), traffic=PROFILED_TRAFFIC["prefill_full"],
-                      traffic_source="ncu capture, 42-layer stack, layer 5")
+                      launches_per_step=len(job.full_layers))
+    rl_prefill["traffic"], rl_prefill["traffic_source"] = profiled_traffic(
+        "prefill_full", "ncu capture, 42-layer stack, layer 5")
     rl_prefill["frac"] = rl_prefill["achieved"] / rl_prefill["peak"]
     rooflines = [rl_prefill]
     kinds = (("full", job.full_layers, "attn_simt_kernel<bf16,512,4,fused> (full-layer decode step: append + "
@@ -438,10 +466,10 @@ def run_ours(args, cfg):
                       peak_kind=f"{peak_src} HBM copy bandwidth", bytes_per_launch=avg_b,
                       avg_launch_ms=avg_t * 1e3, launches_sampled=n_launches,
                       launches_per_step=len(layers) * cfg["decode_steps"],
-                      traffic=PROFILED_TRAFFIC["decode_" + kind],
-                      traffic_source=f"ncu capture, 42-layer stack, layer {'5' if kind == 'full' else '0'}, "
-                                     "first decode step",
                       per_launch_gbs_min=min(per) / 1e9, per_launch_gbs_max=max(per) / 1e9)
+        rl_dec["traffic"], rl_dec["traffic_source"] = profiled_traffic(
+            "decode_" + kind,
+            f"ncu capture, 42-layer stack, layer {'5' if kind == 'full' else '0'}, first decode step")
         rl_dec["frac"] = rl_dec["achieved"] / rl_dec["peak"]
         if kind == "sliding":
             rl_dec["note"] = ("latency-bound: %.1f MB per launch, so the launch and the kernel's dependent "
