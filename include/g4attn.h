@@ -147,7 +147,10 @@ int32_t g4_kv_share_src(int32_t n_layers, int32_t n_shared, const int32_t* is_sl
  * Step a4: fused norm -> RoPE -> KV append for B*T tokens of one layer.
  *   q_in       [B][T][n_heads][head_dim]      raw q projections
  *   k_in, v_in [B][T][n_kv_heads][head_dim]   raw k / v projections; must be
- *              NULL on a shared layer (kv_share_src >= 0), non-NULL otherwise
+ *              NULL on a shared layer (kv_share_src >= 0), non-NULL otherwise.
+ *              A full layer whose v projection is its k projection
+ *              (turbospark-runtime gemma4 `attention_k_eq_v`) passes the raw
+ *              k as v_in too; v is then the weight-less norm of the raw k.
  *   q_norm_w   [head_dim] float32 weight shared by all q heads
  *   k_norm_w   [head_dim] float32 weight shared by all k heads (NULL on a
  *              shared layer).  v has no weight.
@@ -247,7 +250,8 @@ g4_status g4_attn_decode(const g4_layer_params* params, const g4_kv_cache* cache
  * positions[b] = seq_lens[b] - 1 (T = 1) followed by g4_attn_decode on its
  * q_out, without the q_out round trip through memory:
  *   q_in         [B][n_heads][head_dim] raw q of the new token
- *   k_in, v_in   [B][n_kv_heads][head_dim] raw k / v (NULL on a shared layer)
+ *   k_in, v_in   [B][n_kv_heads][head_dim] raw k / v (NULL on a shared layer;
+ *                the same pointer twice for attention_k_eq_v, as above)
  *   q_norm_w, k_norm_w  float32 [head_dim] (k_norm_w NULL on a shared layer)
  * On a layer that owns its cache the new k / v rows are written to position
  * seq_lens[b] - 1 of caches[layer] (row seq_lens[b] - 1, or that mod max_len

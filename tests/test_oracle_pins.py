@@ -656,3 +656,25 @@ def test_attn_output_residual_library_and_special_cases():
     g2 = O.attn_output_residual(h, 7.5 * ao, wo, np.ones(D), 0.0)
     assert np.allclose(g1, g2, rtol=0, atol=1e-12)
     assert np.allclose(np.mean((g1 - h) ** 2, axis=-1), 1.0, rtol=1e-12)
+
+
+def test_k_eq_v_values_are_the_plain_norm_of_the_raw_k():
+    # attention_k_eq_v (the v projection is the k projection): the layer's
+    # raw v is its raw k, so each stored v row is the weight-less RMSNorm of
+    # the raw k row (torch's rms_norm as the library routine), unroped, while
+    # k is normed with its weight and roped as usual
+    B, T, H, Hkv, hd, Lmax = 1, 3, 2, 2, 64, 8
+    r = rng(60)
+    lp = dict(head_dim=hd, theta=1e6, rotary_fraction=0.25, eps=1e-6, dtype=O.F32, kv_share_src=-1)
+    q = r.standard_normal((B, T, H, hd))
+    k = r.standard_normal((B, T, Hkv, hd))
+    qw = 1 + 0.1 * r.standard_normal(hd)
+    kw = 1 + 0.1 * r.standard_normal(hd)
+    pos = np.array([[5, 6, 7]])
+    ck = np.zeros((B, Hkv, Lmax, hd))
+    cv = np.zeros((B, Hkv, Lmax, hd))
+    O.kv_append_normrope(lp, q, k, k, qw, kw, pos, ck, cv)
+    ref_v = torch.nn.functional.rms_norm(torch.from_numpy(k), (hd,), None, 1e-6).numpy()
+    for t in range(T):
+        assert np.allclose(cv[0, :, pos[0, t]], O.store(ref_v[0, t], O.F32), rtol=0, atol=1e-7)
+        assert not np.allclose(ck[0, :, pos[0, t]], cv[0, :, pos[0, t]])
