@@ -360,7 +360,8 @@ g4_status g4_attn_encoder(const g4_layer_params* params, const g4_kv_cache* cach
   a.sliding = sliding;
   a.window = window;
   a.len_cap = c->max_len;
-  a.chunk = sliding ? 2 * window + 1 : T;  // one split holds a query's whole key range
+  // one split holds a query's whole key range (2 window + 1 keys at most, T at most)
+  a.chunk = sliding && 2LL * window + 1 < T ? 2 * window + 1 : T;
   a.nsplit = 1;
   a.scale_log2 = scale_log2;
   return cuda_status(g4::launch_attn_simt(a, params->dtype, s), "float32 encoder launch");
