@@ -162,8 +162,8 @@ int32_t g4_kv_share_src(int32_t n_layers, int32_t n_shared, const int32_t* is_sl
  * The layer's cache is caches[layer] (n_layers entries).  Writes exactly the
  * rows k[b][*][row(positions[b][t])][*] and v[...] for every (b, t); nothing
  * else in the cache changes.  Two tokens of one call that map to the same
- * ring row leave either one there.  RoPE angles are pos * inv_freq[j] with inv_freq held
- * in float32 and the angle reduced in float64.
+ * ring row leave either one there.  RoPE angles are pos * inv_freq[j] with
+ * inv_freq held in float32 and the angle reduced in float64.
  */
 g4_status g4_kv_append_normrope(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
                                 int32_t layer, const void* q_in, const void* k_in, const void* v_in,
