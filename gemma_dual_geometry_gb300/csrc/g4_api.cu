@@ -39,18 +39,20 @@ bool supported_hd(int hd) { return hd == 64 || hd == 128 || hd == 256 || hd == 5
 // Device error word: a kernel that gives up a bounded wait records a code here.
 __device__ int g_device_error = 0;
 
+// Its device address, looked up once per device (with that device current)
+// under a lock, so host threads driving different GPUs each get their own.
 int* device_error_ptr() {
-  static int dev_cached = -1;
-  static int* ptr = nullptr;
+  static std::mutex mu;
+  static int* addr[128] = {};
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
-  if (dev != dev_cached || ptr == nullptr) {
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-    ptr = static_cast<int*>(p);
-    dev_cached = dev;
+    addr[dev] = static_cast<int*>(p);
   }
-  return ptr;
+  return addr[dev];
 }
 
 g4_status check_params(const g4_layer_params* p) {
@@ -381,10 +383,15 @@ namespace {
 // Shared by g4_attn_decode and g4_decode_step: validation, split plan and launch.
 // q is normed+roped (fused == false) or the raw projection (fused == true, with
 // k_in / v_in / weights and the RoPE table of the layer).
+// With clear_tickets the splits' arrival counters in the workspace are
+// zeroed on the stream right before the launch, after every check passed
+// (the built-in scratch of g4_attn_decode_noalloc; a caller's workspace is
+// left zeroed by the previous call instead).
 g4_status decode_common(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers, int32_t layer,
                         const void* q, const void* k_in, const void* v_in, const float* q_norm_w,
                         const float* k_norm_w, bool fused, const int32_t* seq_lens, int32_t B, int32_t max_seq_len,
-                        void* out, void* workspace, size_t workspace_bytes, void* stream) {
+                        void* out, void* workspace, size_t workspace_bytes, void* stream,
+                        bool clear_tickets = false) {
   g4_status st = check_params(params);
   if (st != G4_OK) return st;
   if (B < 0) return fail(G4_ERR_INVALID_ARG, "B %d must be >= 0", B);
@@ -446,6 +453,10 @@ g4_status decode_common(const g4_layer_params* params, const g4_kv_cache* caches
     a.ws_m = reinterpret_cast<float*>(ws + plan.o_bytes);
     a.ws_l = reinterpret_cast<float*>(ws + plan.o_bytes + plan.m_bytes);
     a.tickets = reinterpret_cast<unsigned*>(ws + plan.o_bytes + 2 * plan.m_bytes);
+    if (clear_tickets) {
+      const cudaError_t e = cudaMemsetAsync(a.tickets, 0, plan.t_bytes, static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_status(e, "clearing the decode scratch's arrival counters");
+    }
   }
   if (fused) {
     a.fused = 1;
@@ -509,19 +520,10 @@ g4_status g4_attn_decode_noalloc(const g4_layer_params* params, const g4_kv_cach
   if (scratch == nullptr) return fail(G4_ERR_CUDA, "cannot resolve the built-in decode scratch: %s", cudaGetErrorString(e));
   // Same kernels and split plan as g4_attn_decode, with the split partials in
   // the built-in array.  The partials are written before they are read; the
-  // splits' arrival counters must start at zero, so they are cleared first.
-  if (B >= 1 && max_seq_len >= 1) {
-    const g4::DecodePlan plan = g4::decode_plan(params->layer_type == G4_SLIDING, params->window,
-                                                params->head_dim, params->n_heads, params->n_kv_heads, B,
-                                                max_seq_len);
-    if (plan.t_bytes > 0) {
-      e = cudaMemsetAsync(static_cast<uint8_t*>(scratch) + plan.o_bytes + 2 * plan.m_bytes, 0, plan.t_bytes,
-                          static_cast<cudaStream_t>(stream));
-      if (e != cudaSuccess) return cuda_status(e, "clearing the built-in decode scratch");
-    }
-  }
-  return g4_attn_decode(params, caches, n_layers, layer, q, seq_lens, B, max_seq_len, out, scratch,
-                        kNoAllocScratchBytes, stream);
+  // splits' arrival counters must start at zero, so decode_common clears them
+  // once every argument has been checked, just before the launch.
+  return decode_common(params, caches, n_layers, layer, q, nullptr, nullptr, nullptr, nullptr, false, seq_lens, B,
+                       max_seq_len, out, scratch, kNoAllocScratchBytes, stream, /*clear_tickets=*/true);
 }
 
 const char* g4_last_error(void) { return g_last_error.c_str(); }

@@ -831,13 +831,8 @@ cudaError_t launch_pdl(Kern kern, unsigned grid, unsigned block, size_t smem, cu
 template <typename T, int HD, int G, bool FUSED, int NW>
 cudaError_t launch_simt_hgfw(const AttnSimtArgs& a, long long nblk, cudaStream_t s) {
   using C = SimtCfg<T, HD, G, NW>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<T, HD, G, FUSED, NW>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_B);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t e = set_smem_limit_once<attn_simt_kernel<T, HD, G, FUSED, NW>>(C::SMEM_B);
+  if (e != cudaSuccess) return e;
   return launch_pdl(attn_simt_kernel<T, HD, G, FUSED, NW>, static_cast<unsigned>(nblk), NW * 32, C::SMEM_B, s, a);
 }
 

@@ -6,7 +6,29 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace g4 {
+
+// Raises kernel Kern's dynamic shared-memory limit to `bytes` on the current
+// device.  The attribute belongs to the device, so it is set once per device
+// (and per kernel: Kern is a template argument), under a lock.
+template <auto Kern>
+cudaError_t set_smem_limit_once(int bytes) {
+  static std::mutex mu;
+  static bool done[128] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!done[dev]) {
+    e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    done[dev] = true;
+  }
+  return cudaSuccess;
+}
 
 constexpr int kMaxHalf = 256;  // head_dim / 2 for the widest supported head (512)
 

@@ -746,13 +746,8 @@ bool make_map(CUtensorMap* m, const void* base, const cuuint64_t dims[5], const 
 template <int HD, bool BIDIR>
 cudaError_t launch_hd(const PrefillTcArgs& a, cudaStream_t s) {
   using C = TcCfg<HD>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(prefill_tc_kernel<HD, BIDIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_B);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t e = set_smem_limit_once<prefill_tc_kernel<HD, BIDIR>>(C::SMEM_B);
+  if (e != cudaSuccess) return e;
   CUtensorMap mq, mk, mv, mo;
   const cuuint64_t row_b = static_cast<cuuint64_t>(HD) * 2;
   constexpr cuuint32_t kQBoxChunks = C::QCH > 4 ? C::QCH / 2 : C::QCH;

@@ -13,7 +13,8 @@
  *
  * Sources (page title + item):
  *   cortiq-engine g4e.rs: `rms`, `rms_plain`, `G4eGlobals` (inv_freq tables,
- *     window "current included"), `G4eLayer` (kv_share_src, sliding, hd),
+ *     window counted with the current token), `G4eLayer` (kv_share_src,
+ *     sliding, hd),
  *     `g4e_forward` attention block.
  *   ferrox-models gemma4_engine.rs: `Gemma4Hparams` (head_dim per type,
  *     has_kv, kv_reuse_layer, rope_theta_for, attention_scale = 1.0),
@@ -287,10 +288,11 @@ g4_status g4_decode_step(const g4_layer_params* params, const g4_kv_cache* cache
  * The first call on a device looks up the array's device address (once per
  * device, with that device current); make that first call before any stream
  * capture.  All calls share the one array and it keeps the last call's
- * contents; each call first clears the part that must start at zero (the
- * splits' arrival counters, an asynchronous memset on `stream`).  Calls
- * whose kernels overlap on the GPU (different streams, or several threads)
- * race on the array and must be serialised by the caller.
+ * contents; each call clears the part that must start at zero (the splits'
+ * arrival counters, an asynchronous memset on `stream`) once its arguments
+ * have passed every check, just before its launch, so a refused call writes
+ * nothing.  Calls whose kernels overlap on the GPU (different streams, or
+ * several threads) race on the array and must be serialised by the caller.
  */
 g4_status g4_attn_decode_noalloc(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
                                  int32_t layer, const void* q, const int32_t* seq_lens, int32_t B,

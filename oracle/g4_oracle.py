@@ -152,8 +152,9 @@ def rope_inv_freq(head_dim, theta, rotary_fraction):
     The power is taken in float64 and rounded to float32 once, because the
     pages keep the table as ``Vec<f32>`` (cortiq-engine ``G4eGlobals``) and
     build it in f32 (taconite ``text_attention``).  The denominator is the
-    full head width; the zero tail is the identity under rotation
-    (cortiq-engine ``G4eGlobals`` doc: "the tail is zero, which is identity").
+    full head width; a zero frequency leaves its pair unrotated, so the tail
+    passes through unchanged (cortiq-engine ``g4e.rs``, the ``G4eGlobals``
+    documentation of the global inverse-frequency table).
     """
     half = head_dim // 2
     n_rot = min(rotated_pairs(head_dim, rotary_fraction), half)
@@ -289,9 +290,10 @@ def visible(q_pos, k_pos, layer_type, window):
     """Key at position k_pos is visible from a query at q_pos.
 
     Causal (k <= q) on every layer; a sliding layer also needs q - k < window,
-    i.e. the window counts tokens with the current one included
-    (cortiq-engine ``G4eGlobals``: "Sliding window (tokens, current
-    included)"; turbospark ``kv_start = seq_len - sliding_window``).
+    i.e. the window is counted in tokens and the query's own token is one of
+    them (cortiq-engine ``g4e.rs``, the ``G4eGlobals`` field documentation of
+    the window; turbospark-runtime ``gemma4/attn.rs``, decode:
+    ``kv_start = seq_len - sliding_window``).
     """
     q_pos = np.asarray(q_pos)
     k_pos = np.asarray(k_pos)

@@ -678,3 +678,72 @@ def test_k_eq_v_values_are_the_plain_norm_of_the_raw_k():
     for t in range(T):
         assert np.allclose(cv[0, :, pos[0, t]], O.store(ref_v[0, t], O.F32), rtol=0, atol=1e-7)
         assert not np.allclose(ck[0, :, pos[0, t]], cv[0, :, pos[0, t]])
+
+
+# ---------------------------------------------------------------- the norm -> RoPE composition
+
+def _norm_then_rotate(x, w, pos, inv, eps, rotate=True):
+    """Independent restatement: torch's rms_norm (the library routine, with
+    the weight), then rotate_half as complex multiplication of
+    x_j + i x_{j+hd/2} by exp(i pos inv_freq_j)."""
+    hd = x.shape[-1]
+    xn = torch.nn.functional.rms_norm(torch.from_numpy(np.asarray(x, np.float64)), (hd,),
+                                      None if w is None else torch.from_numpy(np.asarray(w, np.float64)),
+                                      eps).numpy()
+    if not rotate:
+        return xn
+    z = xn[..., :hd // 2] + 1j * xn[..., hd // 2:]
+    zr = z * np.exp(1j * np.asarray(pos, np.float64)[..., None] * inv.astype(np.float64))
+    return np.concatenate([zr.real, zr.imag], axis=-1)
+
+
+@pytest.mark.parametrize("hd,theta,frac", [(256, 1e4, 1.0), (512, 1e6, 0.25), (64, 1e4, 1.0), (128, 1e6, 0.25)])
+@pytest.mark.parametrize("dtype", [O.F32, O.BF16])
+def test_normrope_composition_norm_weight_then_rotation(hd, theta, frac, dtype):
+    # The attention block of cortiq-engine g4e.rs `g4e_forward` and taconite
+    # model.rs `text_attention`: q and k are RMS-normed with their own
+    # weight (q_norm / k_norm) and then roped; v gets the weight-less norm
+    # and no rotation.  Checked against torch's rms_norm followed by complex
+    # rotation, on q / k / v rows at positions from 0 to 131071, through both
+    # normrope_* and the append (which writes the cache and returns q_out).
+    r = rng(70 + hd)
+    B, T, H, Hkv, Lmax = 2, 3, 4, 2, 8
+    eps = 1e-6
+    q = r.standard_normal((B, T, H, hd))
+    k = r.standard_normal((B, T, Hkv, hd))
+    v = r.standard_normal((B, T, Hkv, hd))
+    qw = 1 + 0.1 * r.standard_normal(hd)
+    kw = 1 + 0.1 * r.standard_normal(hd)
+    pos = np.array([[0, 9, 131071], [4096, 4098, 5]])  # distinct rows mod 8
+    inv = O.rope_inv_freq(hd, theta, frac)
+    ref_q = _norm_then_rotate(q, qw, pos[..., None], inv, eps)
+    ref_k = _norm_then_rotate(k, kw, pos[..., None], inv, eps)
+    ref_v = _norm_then_rotate(v, None, pos[..., None], inv, eps, rotate=False)
+    # normrope_q / normrope_kv
+    assert np.allclose(O.normrope_q(q, qw, pos, hd, theta, frac, eps), ref_q, rtol=0, atol=1e-12)
+    kn, vn = O.normrope_kv(k, v, kw, pos, hd, theta, frac, eps)
+    assert np.allclose(kn, ref_k, rtol=0, atol=1e-12)
+    assert np.allclose(vn, ref_v, rtol=0, atol=1e-12)
+    # the append: q_out with q's weight, cache k with k's weight, v unroped,
+    # each rounded as stored (round_bf16 is pinned against torch above)
+    lp = dict(head_dim=hd, theta=theta, rotary_fraction=frac, eps=eps, dtype=dtype, kv_share_src=-1)
+    ck = np.zeros((B, Hkv, Lmax, hd))
+    cv = np.zeros((B, Hkv, Lmax, hd))
+    ring_cap = Lmax
+    q_out = O.kv_append_normrope(lp, q, k, v, qw, kw, pos, ck, cv, ring=True)
+    tol = 1e-6 if dtype == O.F32 else 2.0 ** -7
+    assert np.allclose(q_out, ref_q, rtol=tol, atol=1e-6)
+    for b in range(B):
+        for t in range(T):
+            row = int(pos[b, t]) % ring_cap
+            assert np.allclose(ck[b, :, row], ref_k[b, t], rtol=tol, atol=1e-6)
+            assert np.allclose(cv[b, :, row], ref_v[b, t], rtol=tol, atol=1e-6)
+    # The mistakes this pin separates from the right composition: RoPE
+    # before the weighted norm (the weight is per element, so the two do not
+    # commute), the weights of q and k exchanged, v roped.
+    rope_first = _norm_then_rotate(q, None, pos[..., None], inv, eps) * qw
+    swapped_q = _norm_then_rotate(q, kw, pos[..., None], inv, eps)
+    roped_v = _norm_then_rotate(v, None, pos[..., None], inv, eps)
+    assert not np.allclose(rope_first, ref_q, rtol=0, atol=1e-3)
+    assert not np.allclose(swapped_q, ref_q, rtol=0, atol=1e-3)
+    assert not np.allclose(roped_v, ref_v, rtol=0, atol=1e-3)
