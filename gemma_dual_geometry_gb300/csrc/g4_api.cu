@@ -371,7 +371,7 @@ g4_status g4_attn_encoder(const g4_layer_params* params, const g4_kv_cache* cach
 
 size_t g4_attn_decode_workspace_size(const g4_layer_params* params, int32_t B, int32_t max_seq_len) {
   if (check_params(params) != G4_OK || B < 1 || max_seq_len < 1) return 0;
-  return g4::decode_plan(params->layer_type == G4_SLIDING, params->window, params->head_dim, params->n_heads,
+  return g4::decode_plan(params->dtype, params->layer_type == G4_SLIDING, params->window, params->head_dim, params->n_heads,
                          params->n_kv_heads, B, max_seq_len)
       .ws_bytes;
 }
@@ -417,7 +417,7 @@ g4_status decode_common(const g4_layer_params* params, const g4_kv_cache* caches
   if (max_seq_len < 1 || (!c->ring && max_seq_len > c->max_len))
     return fail(G4_ERR_CAPACITY, "max_seq_len %d outside [1, cache length %d]", max_seq_len, c->max_len);
   if (B == 0) return ok();
-  const g4::DecodePlan plan = g4::decode_plan(params->layer_type == G4_SLIDING, params->window, params->head_dim,
+  const g4::DecodePlan plan = g4::decode_plan(params->dtype, params->layer_type == G4_SLIDING, params->window, params->head_dim,
                                               params->n_heads, params->n_kv_heads, B, max_seq_len);
   if (workspace_bytes < plan.ws_bytes)
     return fail(G4_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", workspace_bytes, plan.ws_bytes);
@@ -478,6 +478,8 @@ g4_status decode_common(const g4_layer_params* params, const g4_kv_cache* caches
       a.inv_freq[j] =
           j < n_rot ? static_cast<float>(pow(static_cast<double>(params->theta), -2.0 * j / a.hd)) : 0.0f;
   }
+  if (plan.win)
+    return cuda_status(g4::launch_decode_win(a, static_cast<cudaStream_t>(stream)), "windowed decode launch");
   return cuda_status(g4::launch_attn_simt(a, params->dtype, static_cast<cudaStream_t>(stream)), "decode launch");
 }
 
@@ -506,7 +508,7 @@ g4_status g4_attn_decode_noalloc(const g4_layer_params* params, const g4_kv_cach
   g4_status st = check_params(params);
   if (st != G4_OK) return st;
   if (B >= 1 && max_seq_len >= 1) {
-    const g4::DecodePlan plan = g4::decode_plan(params->layer_type == G4_SLIDING, params->window,
+    const g4::DecodePlan plan = g4::decode_plan(params->dtype, params->layer_type == G4_SLIDING, params->window,
                                                 params->head_dim, params->n_heads, params->n_kv_heads, B,
                                                 max_seq_len);
     if (plan.ws_bytes > kNoAllocScratchBytes)

@@ -114,16 +114,29 @@ struct PrefillTcArgs {
 };
 cudaError_t launch_prefill_tc(const PrefillTcArgs& a, cudaStream_t s);
 
+// Step a6 (bf16) for key spans of at most kMaxWinSplits x 64 keys per
+// (sequence, kv head): one cluster of 64-key CTAs per (sequence, kv head),
+// merged through distributed shared memory; no workspace.  Takes the
+// AttnSimtArgs of a decode (mode 0, T = 1) with chunk = 64 and nsplit =
+// decode_win_splits(span).  Used when its CTAs fit one wave
+// (decode_win_eligible, units = batch x kv heads).
+constexpr int kMaxWinSplits = 8;
+bool decode_win_eligible(int dtype, int hd, int group, int span, int units);
+int decode_win_splits(int span);
+cudaError_t launch_decode_win(const AttnSimtArgs& a, cudaStream_t s);
+
 // Decode split plan shared by the workspace query and the launch.
 // Workspace layout: ws_o, then ws_m, ws_l, tickets, each 256-byte aligned.
+// win = 1: the windowed cluster kernel (launch_decode_win), no workspace.
 constexpr int kMaxSplits = 128;
 struct DecodePlan {
   int chunk;
   int nsplit;
+  int win;
   size_t o_bytes, m_bytes, t_bytes;  // sizes of the four regions (ws_m and ws_l share m_bytes)
   size_t ws_bytes;
 };
-DecodePlan decode_plan(int sliding, int window, int hd, int H, int Hkv, int B, int max_seq_len);
+DecodePlan decode_plan(int dtype, int sliding, int window, int hd, int H, int Hkv, int B, int max_seq_len);
 int sm_count();  // SMs of the current device
 
 }  // namespace g4

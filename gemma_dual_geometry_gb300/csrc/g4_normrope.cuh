@@ -379,4 +379,160 @@ __device__ __forceinline__ float inv_rms_f32(float sumsq, int hd, float eps) {
   return __frsqrt_rn(fmaf(sumsq, 1.0f / static_cast<float>(hd), eps));
 }
 
+// ---------------------------------------------------------------- whole rows
+// A head row held by one warp: lane l owns pieces l + 32c (c < NPC) of PE
+// consecutive elements (16-byte pieces where the row is wide enough).
+
+// Lane l's elements of a row: pieces l + 32c (c < NPC) of PE elements.
+template <typename T, int NPC, int PE>
+__device__ __forceinline__ void load_row(const T* row, int lane, float* f) {
+#pragma unroll
+  for (int c = 0; c < NPC; ++c) load_elems<PE>(row + (lane + 32 * c) * PE, f + c * PE);
+}
+
+template <typename T, int NPC, int PE>
+__device__ __forceinline__ void store_row(T* row, int lane, const float* f) {
+#pragma unroll
+  for (int c = 0; c < NPC; ++c) store_elems<PE>(row + (lane + 32 * c) * PE, f + c * PE);
+}
+
+template <int N>
+__device__ __forceinline__ void to_f2(const float* f, float2 (&x)[N / 2]) {
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) x[i] = make_float2(f[2 * i], f[2 * i + 1]);
+}
+
+template <typename T, int NPC, int PE>
+__device__ __forceinline__ void load_row_f2(const T* row, int lane, float2 (&x)[NPC * PE / 2]) {
+  float f[NPC * PE];
+  load_row<T, NPC, PE>(row, lane, f);
+  to_f2<NPC * PE>(f, x);
+}
+
+// Round through the storage type (what a stored row would hold).
+template <typename T>
+__device__ __forceinline__ float through(float x) {
+  if constexpr (sizeof(T) == 2) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+  } else {
+    return x;
+  }
+}
+
+// RMSNorm (optional weight) then rotate_half RoPE of one row held in the lane
+// layout above (src: the same row in memory; wf: the lane's weights, from w,
+// or ones when w is null), at position pos; the partner
+// of element d is d +- HD/2, which is the same lane (NPC >= 2) or lane ^ 16
+// (NPC == 1).  bf16 results are the correctly rounded real values
+// (g4_normrope.cuh), the ones the append kernel stores, decided in three
+// stages as there: float32 with Ziv's test; the float inverse rms times the
+// inner products in double-float for the values left open; the row's
+// double-float inverse rms for the rest.  s_cos / s_sin hold cos and sin of
+// the HD/2 pairs.
+template <typename T, int HD, int NPC, int PE>
+__device__ __forceinline__ void norm_rope_row(float* f, const float* wf, const T* src, const float* w, bool rope,
+                                              const DF* s_cos, const DF* s_sin, int n_rot, float eps, int lane) {
+  constexpr int EL = NPC * PE;
+  constexpr bool kBF16 = sizeof(T) == 2;
+  constexpr float kErrY = normrope_err_y<EL>();
+  constexpr float kErrAB = normrope_err_pair(kDFTrigErrUnits);
+  constexpr float kErrO = normrope_err_out<EL>();
+  constexpr float kErrR = normrope_err_r<EL>();
+  const float sf = row_sumsq_f32<EL>(f);
+  const float r = inv_rms_f32(sf, HD, eps);
+  // raw partner values and weights
+  float fp[EL], wp[EL];
+  if constexpr (NPC >= 2) {
+#pragma unroll
+    for (int c = 0; c < NPC; ++c)
+#pragma unroll
+      for (int e = 0; e < PE; ++e) {
+        fp[c * PE + e] = f[((c + NPC / 2) % NPC) * PE + e];
+        wp[c * PE + e] = wf[((c + NPC / 2) % NPC) * PE + e];
+      }
+  } else {
+#pragma unroll
+    for (int e = 0; e < PE; ++e) {
+      fp[e] = __shfl_xor_sync(0xffffffffu, f[e], 16);
+      wp[e] = __shfl_xor_sync(0xffffffffu, wf[e], 16);
+    }
+  }
+  float o[EL];
+  uint32_t need = 0;
+#pragma unroll
+  for (int c = 0; c < NPC; ++c) {
+#pragma unroll
+    for (int e = 0; e < PE; ++e) {
+      const int i = c * PE + e;
+      const int d = (lane + 32 * c) * PE + e;
+      const bool lower = d < HD / 2;
+      const int j = lower ? d : d - HD / 2;
+      const bool rot = rope && j < n_rot;
+      const float2 t = rot ? make_float2(s_cos[j].h, s_sin[j].h) : make_float2(1.0f, 0.0f);
+      float oa, ob;
+      bool na, nb;
+      if (lower) {
+        normrope_pair_fast(f[i], wf[i], fp[i], wp[i], r, rot, t.x, t.y, kErrY, kErrAB, kErrO, oa, ob, na, nb);
+        o[i] = oa;
+        need |= (na ? 1u : 0u) << i;
+      } else {
+        normrope_pair_fast(fp[i], wp[i], f[i], wf[i], r, rot, t.x, t.y, kErrY, kErrAB, kErrO, oa, ob, na, nb);
+        o[i] = ob;
+        need |= (nb ? 1u : 0u) << i;
+      }
+    }
+  }
+  if constexpr (kBF16) {
+    if (__any_sync(0xffffffffu, need != 0)) {
+      // Stage 2, lane by lane, one open value per pass (operands reloaded).
+      uint32_t open = 0;
+#pragma unroll 1
+      for (uint32_t left = need; left != 0; left &= left - 1) {
+        const int i = __ffs(left) - 1;
+        const int d = (lane + 32 * (i / PE)) * PE + i % PE;
+        const bool lower = d < HD / 2;
+        const int j = lower ? d : d - HD / 2;
+        const int other = lower ? d + HD / 2 : d - HD / 2;
+        const float xs = static_cast<float>(src[d]);
+        DF inner = two_prod(xs, w != nullptr ? w[d] : 1.0f);
+        float mag = fabsf(inner.h);
+        if (rope && j < n_rot) {
+          const DF po = two_prod(static_cast<float>(src[other]), w != nullptr ? w[other] : 1.0f);
+          mag += fabsf(po.h);
+          inner = df_add(df_mul(inner, s_cos[j]), df_mul(po, lower ? df_neg(s_sin[j]) : s_sin[j]));
+        }
+        const DF v = df_mul_f(inner, r);
+        if (fabsf((v.h - bf16_midpoint(v.h)) + v.l) > fmaf(kErrR, fabsf(v.h), 0x1.0p-40f * r * mag)) {
+          const float val = df_round_bf16(v);
+#pragma unroll
+          for (int k = 0; k < EL; ++k)
+            if (k == i) o[k] = val;
+        } else {
+          open |= 1u << i;
+        }
+      }
+      // Stage 3: the row's double-float inverse rms.
+      if (__any_sync(0xffffffffu, open != 0)) {
+        const DF rd = inv_rms_df(row_sumsq_split<EL, HD>(f, sf), HD, eps);
+#pragma unroll
+        for (int c = 0; c < NPC; ++c) {
+#pragma unroll
+          for (int e = 0; e < PE; ++e) {
+            const int i = c * PE + e;
+            if (open & (1u << i)) {
+              const int d = (lane + 32 * c) * PE + e;
+              const bool lower = d < HD / 2;
+              const int j = lower ? d : d - HD / 2;
+              o[i] = normrope_exact_bf16(f[i], wf[i], fp[i], wp[i], rd, rope && j < n_rot, lower, s_cos[j], s_sin[j]);
+            }
+          }
+        }
+      }
+    }
+  }
+  // the stored value (certified float32 values still need their rounding)
+#pragma unroll
+  for (int i = 0; i < EL; ++i) f[i] = through<T>(o[i]);
+}
+
 }  // namespace g4

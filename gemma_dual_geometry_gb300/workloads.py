@@ -18,7 +18,8 @@ The five workloads are the ones the attention path is specified on:
   sliding layer.
 
 ``stack42_bf16_dec8`` is ``stack42_bf16`` with 8 decode steps, for launch lists
-taken under a profiler.
+taken under a profiler; ``stack42_bf16_b2`` is the stack at batch 2, the small
+case for counter captures.
 
 Values: q/k/v and cache contents ~ N(0, 1); norm weights ~ 1 + 0.1 N(0, 1)
 (float32).  bf16 workloads round the float32 draws to bf16 (torch's RNE cast).
@@ -57,6 +58,13 @@ CONFIGS = {
     # 128-step figures are the decode launches' times x 16.
     "stack42_bf16_dec8": dict(
         B=8, T=4096, decode_steps=8, H=8, Hkv=2, dtype=BF16, seed=3,
+        types=[FULL if (i + 1) % 6 == 0 else SLIDING for i in range(42)], n_shared=18,
+        geom={SLIDING: SLIDING_GEOM_BF16, FULL: FULL_GEOM_BF16}),
+    # The stack at batch 2 with a 2-step decode phase: the small case that
+    # counter captures under a profiler run on (about 2.5 GB on the device);
+    # per-launch figures scale to batch 8 by the sequences processed.
+    "stack42_bf16_b2": dict(
+        B=2, T=4096, decode_steps=2, H=8, Hkv=2, dtype=BF16, seed=3,
         types=[FULL if (i + 1) % 6 == 0 else SLIDING for i in range(42)], n_shared=18,
         geom={SLIDING: SLIDING_GEOM_BF16, FULL: FULL_GEOM_BF16}),
     # decode_bf16 with the sliding layer's cache as a ring of one window

@@ -161,6 +161,15 @@ def test_decode_validation_and_workspace(L):
     assert dec(B=0) == G.G4_OK
     # a sliding layer whose window is no longer than the minimum split needs no workspace
     assert G.g4_attn_decode_workspace_size(_params(window=64), 64, 8192) == 0    # one 64-key split
+    # bf16 spans of at most 512 keys (head_dim <= 256) merge their splits in a
+    # cluster when its CTAs fit one wave: no workspace; longer windows, head_dim
+    # 512, float32 and more (sequence, kv head) pairs use the split kernel's
+    assert G.g4_attn_decode_workspace_size(_params(window=512), 8, 8192) == 0       # 16 clusters of 8
+    assert G.g4_attn_decode_workspace_size(_params(layer_type=G.G4_FULL, window=0), 8, 512) == 0
+    assert G.g4_attn_decode_workspace_size(_params(window=512), 64, 8192) > 0      # 1024 CTAs: split kernel
+    assert G.g4_attn_decode_workspace_size(_params(window=1024), 8, 8192) > 0
+    assert G.g4_attn_decode_workspace_size(_params(window=512, dtype=G.G4_F32), 8, 8192) > 0
+    assert G.g4_attn_decode_workspace_size(_params(layer_type=G.G4_FULL, window=0), 8, 513) > 0
     assert L.g4_attn_decode_workspace_size(None, 64, 8192) == 0
 
 

@@ -117,3 +117,15 @@ def test_reduce_over_two_gloo_ranks():
 def test_single_process_reduce_is_identity():
     assert bench.reduce_max(3.25) == 3.25
     assert bench.dist_env()[1] in (1, int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def test_oracle_baseline_pool_runs_on_several_cores():
+    # the CPU baseline's sample on a process pool (spawn), on the tiny stack:
+    # every layer's append and (layer, query group) attention tasks run, and
+    # the line reports the workers it used
+    res = bench.oracle_worker(dict(workload="tiny_fp32_stack", steps=1, warmup=0, n_query=8, append_chunk=16,
+                                   query_group=4, max_cores=2))
+    assert res["cores"] == min(2, len(os.sched_getaffinity(0)))
+    (step,) = res["steps"]
+    assert step["t_append"] > 0 and step["t_attn"] > 0 and step["cpu_s"] > 0
+    assert step["per_token_s"] == pytest.approx(step["t_append"] / 16 + step["t_attn"] / 8)

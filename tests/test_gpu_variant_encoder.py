@@ -68,7 +68,9 @@ def run_encoder(geo, B, T, seed, Lmax=None):
         assert np.array_equal(gk[:, :, :T], ok[:, :, :T]) and np.array_equal(gv[:, :, :T], ov[:, :, :T])
     assert np.isnan(gk[:, :, T:]).all() and np.isnan(gv[:, :, T:]).all()
     ref = O.attention_bidirectional(gq, gk, gv, T, Hkv, geo["layer_type"], geo["window"], geo["attn_scale"])
-    run_encoder.last = dict(table=table, q_out=q_out, out=out)
+    # the table holds raw device pointers: the cache tensors must stay alive
+    # as long as it is used (a later launch on it would read freed memory)
+    run_encoder.last = dict(table=table, q_out=q_out, out=out, caches=(ck, cv))
     return f64(out), ref
 
 

@@ -92,8 +92,9 @@ def _no_alloc(x):
 def test_no_alloc_decode_matches_workspace_decode_on_two_calls_in_a_row():
     # call 1: full layer, head_dim 512, ragged lengths (many splits)
     a = _decode_inputs(geometry(W.FULL, 512), [1, 130, 2047, 3000, 777], 3008, seed=41)
-    # call 2: sliding layer, head_dim 256, other shapes and lengths
-    b = _decode_inputs(geometry(W.SLIDING, 256, window=512), [5, 600, 2500], 2504, seed=42)
+    # call 2: sliding layer, head_dim 256, a window of 1024 keys (spans above
+    # 512 keys go through the split kernel and its scratch), other lengths
+    b = _decode_inputs(geometry(W.SLIDING, 256, window=1024), [5, 600, 2500], 2504, seed=42)
     ref_a, ws_a = _with_workspace(a)
     ref_b, ws_b = _with_workspace(b)
     assert ws_a > 0 and ws_b > 0          # both plans really use split-KV scratch
