@@ -601,10 +601,81 @@ class LayerJob:
         return 2 * self.n
 
 
+class ProjJob:
+    """The projection workloads (qkv_proj_bf16, out_proj_bf16): one step is
+    the fused projection of every layer of the workload, each launch timed
+    with CUDA events like LayerJob's attention launches."""
+
+    decode = False
+    encoder = False
+
+    def __init__(self, cfg, device):
+        import torch
+
+        from gemma_dual_geometry_gb300 import g4attn as G
+        from gemma_dual_geometry_gb300 import workloads as W
+        from gemma_dual_geometry_gb300.stack import AttnStack
+
+        self.cfg, self.torch, self.G = cfg, torch, G
+        self.B, self.T, self.D = cfg["B"], cfg["T"], cfg["D"]
+        self.M = self.B * self.T
+        self.kind = cfg["proj"]
+        self.st = AttnStack(cfg, self.T, device=device) if self.kind == "qkv" else None
+        self.geo = [W.layer_geometry(cfg, l) for l in range(len(cfg["types"]))]
+        self.n = len(self.geo)
+        self.X = [W.projection_inputs(cfg, l, device=device) for l in range(self.n)]
+        if self.kind == "qkv":
+            self.pos = torch.arange(self.T, dtype=torch.int32, device=device).repeat(self.B, 1).contiguous()
+            self.qo = [torch.empty((self.M, cfg["H"], g["head_dim"]), dtype=torch.bfloat16, device=device)
+                       for g in self.geo]
+        else:
+            self.out = [torch.empty((self.M, self.D), dtype=torch.bfloat16, device=device) for _ in self.geo]
+        self.events = {l: [] for l in range(self.n)}
+
+    def step(self, record=False):
+        torch, G = self.torch, self.G
+        for l in range(self.n):
+            x = self.X[l]
+            ev = None
+            if record:
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ev[0].record()
+            if self.kind == "qkv":
+                G.g4_qkv_project_append(self.st.params[l], self.st.table, l, x["x"], self.D, x["w"], x["q_norm_w"],
+                                        x["k_norm_w"], self.pos, self.B, self.T, self.qo[l])
+            else:
+                K = self.cfg["H"] * self.geo[l]["head_dim"]
+                G.g4_attn_out_residual(x["ao"], self.M, K, x["w"], self.D, x["post_w"], self.geo[l]["eps"], x["h"],
+                                       self.out[l])
+            if ev is not None:
+                ev[1].record()
+                self.events[l].append(ev)
+
+    def layer_work(self, l):
+        """Algorithmic flops of one launch: 2 M N K of the GEMM."""
+        hd, H, Hkv = self.geo[l]["head_dim"], self.cfg["H"], self.cfg["Hkv"]
+        if self.kind == "qkv":
+            return 2.0 * self.M * (H + 2 * Hkv) * hd * self.D
+        return 2.0 * self.M * self.D * H * hd
+
+    def label(self, l):
+        g = self.geo[l]
+        if self.kind == "qkv":
+            return (f"gemm_tc_kernel<{g['head_dim']},0>: q/k/v projection (M {self.M}, N "
+                    f"{(self.cfg['H'] + 2 * self.cfg['Hkv']) * g['head_dim']}, K {self.D}) + input norm + per-head "
+                    f"norm / RoPE / append")
+        return (f"gemm_tc_kernel<256,1>: o_proj (M {self.M}, N {self.D}, K {self.cfg['H'] * g['head_dim']}) + "
+                f"post-attention norm + residual")
+
+    def launches_per_step(self):
+        return self.n
+
+
 L2_FLUSH_BYTES = 256 << 20   # written before every step of the per-workload measurements (> the 129 MB L2)
 # The workloads measured after the stack in the default run (one entry each
 # under "configs" of the JSON line, each with its own clock record).
-EXTRA_WORKLOADS = ("prefill_bf16", "decode_bf16", "longctx_decode_bf16", "ring_decode_bf16", "encoder_bf16")
+EXTRA_WORKLOADS = ("prefill_bf16", "decode_bf16", "longctx_decode_bf16", "ring_decode_bf16", "encoder_bf16",
+                   "qkv_proj_bf16", "out_proj_bf16")
 
 
 def measure_layer_workload(name, args, dev, min_timed_s=0.6, max_steps=4000):
@@ -620,7 +691,7 @@ def measure_layer_workload(name, args, dev, min_timed_s=0.6, max_steps=4000):
     import torch
     from gemma_dual_geometry_gb300 import workloads as W
     cfg = W.CONFIGS[name]
-    job = LayerJob(cfg, dev)
+    job = ProjJob(cfg, dev) if cfg.get("proj") else LayerJob(cfg, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     for _ in range(max(3, args.warmup)):
         flush.zero_()
@@ -654,7 +725,7 @@ def measure_layer_workload(name, args, dev, min_timed_s=0.6, max_steps=4000):
     for l in range(job.n):
         t = statistics.mean(a.elapsed_time(b) for a, b in job.events[l]) * 1e-3
         w = job.layer_work(l)
-        g = job.st.geo[l]
+        g = job.geo[l] if isinstance(job, ProjJob) else job.st.geo[l]
         r = dict(layer=l, layer_type="sliding" if g["layer_type"] == 0 else "full", head_dim=g["head_dim"],
                  avg_launch_ms=t * 1e3, launches_sampled=len(job.events[l]), traffic=None)
         if job.decode:
@@ -664,7 +735,8 @@ def measure_layer_workload(name, args, dev, min_timed_s=0.6, max_steps=4000):
                      bytes_per_launch=w, peak_kind=f"{src} HBM copy bandwidth")
         else:
             ach = w / t / 1e12
-            r.update(kernel="tcgen05 " + ("encoder" if job.encoder else "prefill") + " attention", bound="tensor",
+            r.update(kernel=job.label(l) if isinstance(job, ProjJob) else
+                     "tcgen05 " + ("encoder" if job.encoder else "prefill") + " attention", bound="tensor",
                      achieved=ach, peak=peaks["bf16_tflops"], unit="TFLOP/s", frac=ach / peaks["bf16_tflops"],
                      frac_of_sustained=ach / peaks["bf16_tflops_sustained"], flops_per_launch=w,
                      peak_kind=f"{src} bf16 dense, burst (kernel timed alone; frac_of_sustained against the "
@@ -677,6 +749,12 @@ def measure_layer_workload(name, args, dev, min_timed_s=0.6, max_steps=4000):
         if cfg.get("ring"):
             what += ", sliding cache a ring of one window (512 rows)"
         vdef = "algorithmic K/V + q + out bytes of every layer's decode step / step time"
+    elif isinstance(job, ProjJob):
+        value, unit = job.M * steps * world / total, "tokens/s"
+        what = (f"B={job.B} T={job.T} D={job.D}, " + ("q/k/v projection fused into the norm / RoPE / append"
+                                                      if job.kind == "qkv" else
+                                                      "o_proj + post-attention norm + residual"))
+        vdef = "B*T tokens / step time (the fused projection of every layer)"
     else:
         value, unit = job.B * job.T * steps * world / total, "tokens/s"
         what = f"B={job.B} {'encoder (bidirectional)' if job.encoder else 'prefill'}, T={job.T}"

@@ -21,7 +21,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libg4attn.so")
-SOURCES = ["g4_api.cu", "g4_append.cu", "g4_attn_simt.cu", "g4_decode_win.cu", "g4_prefill_tc.cu"]
+SOURCES = ["g4_api.cu", "g4_append.cu", "g4_attn_simt.cu", "g4_decode_win.cu", "g4_gemm_tc.cu", "g4_prefill_tc.cu"]
 HEADERS = ["g4_device.cuh", "g4_internal.h", "g4_normrope.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -528,6 +528,100 @@ g4_status g4_attn_decode_noalloc(const g4_layer_params* params, const g4_kv_cach
                        max_seq_len, out, scratch, kNoAllocScratchBytes, stream, /*clear_tickets=*/true);
 }
 
+g4_status g4_qkv_project_append(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
+                                int32_t layer, const void* x, int32_t D, const void* w_qkv, const float* q_norm_w,
+                                const float* k_norm_w, const int32_t* positions, int32_t B, int32_t T, void* q_out,
+                                void* stream) {
+  g4_status st = check_params(params);
+  if (st != G4_OK) return st;
+  if (params->dtype != G4_BF16)
+    return fail(G4_ERR_UNSUPPORTED, "the fused projection runs on the bf16 tensor cores only");
+  if (B < 0 || T < 0) return fail(G4_ERR_INVALID_ARG, "B %d and T %d must be >= 0", B, T);
+  if (D < 64 || D % 64 != 0) return fail(G4_ERR_UNSUPPORTED, "D %d must be a positive multiple of 64", D);
+  if (x == nullptr || w_qkv == nullptr || q_norm_w == nullptr || positions == nullptr || q_out == nullptr)
+    return fail(G4_ERR_INVALID_ARG, "x, w_qkv, q_norm_w, positions and q_out must be non-NULL");
+  if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(q_out) || !aligned16(q_norm_w))
+    return fail(G4_ERR_INVALID_ARG, "x, w_qkv, q_norm_w and q_out must be 16-byte aligned");
+  const bool shared = params->kv_share_src >= 0;
+  g4::GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  if (shared) {
+    if (k_norm_w != nullptr)
+      return fail(G4_ERR_INVALID_ARG, "layer %d shares the cache of layer %d: k_norm_w must be NULL", layer,
+                  params->kv_share_src);
+    if (layer < 0 || layer >= n_layers) return fail(G4_ERR_INVALID_ARG, "layer %d outside [0, %d)", layer, n_layers);
+  } else {
+    if (k_norm_w == nullptr || !aligned16(k_norm_w))
+      return fail(G4_ERR_INVALID_ARG, "layer %d owns its cache: k_norm_w must be non-NULL and 16-byte aligned", layer);
+    const g4_kv_cache* c = nullptr;
+    st = resolve_src(params, caches, n_layers, layer, &c);
+    if (st != G4_OK) return st;
+    if (c->batch < B) return fail(G4_ERR_CAPACITY, "cache batch %d < B %d", c->batch, B);
+    a.cache_k = c->k;
+    a.cache_v = c->v;
+    a.max_len = c->max_len;
+    a.ring = c->ring;
+    a.k_w = k_norm_w;
+  }
+  const long long M = static_cast<long long>(B) * T;
+  if (M == 0) return ok();
+  if (M > 0x7fffffffLL - 128) return fail(G4_ERR_INVALID_ARG, "B * T too large");
+  const int hd = params->head_dim;
+  a.epi = 0;
+  a.M = static_cast<int>(M);
+  a.K = D;
+  a.N = (params->n_heads + (shared ? 0 : 2 * params->n_kv_heads)) * hd;
+  a.B = B;
+  a.T = T;
+  a.H = params->n_heads;
+  a.Hkv = params->n_kv_heads;
+  a.hd = hd;
+  a.eps = params->eps;
+  a.eps_in = params->eps;
+  a.q_w = q_norm_w;
+  a.positions = positions;
+  a.q_out = q_out;
+  const int half = hd / 2;
+  int n_rot = static_cast<int>(floor(static_cast<double>(hd) * static_cast<double>(params->rotary_fraction) / 2.0));
+  if (n_rot > half) n_rot = half;
+  a.n_rot = n_rot;
+  for (int j = 0; j < half; ++j)
+    a.inv_freq[j] = j < n_rot ? static_cast<float>(pow(static_cast<double>(params->theta), -2.0 * j / hd)) : 0.0f;
+  int* err = device_error_ptr();
+  if (err == nullptr) return fail(G4_ERR_CUDA, "cannot resolve the device error word");
+  a.err = err;
+  return cuda_status(g4::launch_gemm_tc(a, x, w_qkv, static_cast<cudaStream_t>(stream)), "projection launch");
+}
+
+g4_status g4_attn_out_residual(const void* ao, int32_t M, int32_t K, const void* w_o, int32_t D,
+                               const float* post_norm_w, float eps, const void* h, void* out, void* stream) {
+  if (M < 0) return fail(G4_ERR_INVALID_ARG, "M %d must be >= 0", M);
+  if (K < 64 || K % 64 != 0) return fail(G4_ERR_UNSUPPORTED, "K %d must be a positive multiple of 64", K);
+  if (D < 256 || D % 256 != 0 || D > 2048)
+    return fail(G4_ERR_UNSUPPORTED, "D %d must be a multiple of 256 in [256, 2048]", D);
+  if (!(eps >= 0.0f) || !isfinite(eps)) return fail(G4_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (ao == nullptr || w_o == nullptr || post_norm_w == nullptr || h == nullptr || out == nullptr)
+    return fail(G4_ERR_INVALID_ARG, "ao, w_o, post_norm_w, h and out must be non-NULL");
+  if (!aligned16(ao) || !aligned16(w_o) || !aligned16(h) || !aligned16(out))
+    return fail(G4_ERR_INVALID_ARG, "ao, w_o, h and out must be 16-byte aligned");
+  if (M == 0) return ok();
+  if (M > 0x7fffffff - 128) return fail(G4_ERR_INVALID_ARG, "M too large");
+  int* err = device_error_ptr();
+  if (err == nullptr) return fail(G4_ERR_CUDA, "cannot resolve the device error word");
+  g4::GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.epi = 1;
+  a.M = M;
+  a.K = K;
+  a.N = D;
+  a.err = err;
+  a.eps = eps;
+  a.h = h;
+  a.out = out;
+  a.post_w = post_norm_w;
+  return cuda_status(g4::launch_gemm_tc(a, ao, w_o, static_cast<cudaStream_t>(stream)), "o_proj launch");
+}
+
 const char* g4_last_error(void) { return g_last_error.c_str(); }
 
 int32_t g4_take_device_error(void) {

@@ -125,6 +125,37 @@ bool decode_win_eligible(int dtype, int hd, int group, int span, int units);
 int decode_win_splits(int span);
 cudaError_t launch_decode_win(const AttnSimtArgs& a, cudaStream_t s);
 
+// The projections around the path on the tcgen05 tensor cores: a bf16 GEMM
+// out[M][N] = A[M][K] . Bw[N][K]^T (both operands K-major) whose epilogue is
+//   epi 0: the q / k / v projections of a layer (A = the layer input x, Bw =
+//          the stacked q, k, v rows with the attention-norm weight folded in):
+//          the input RMSNorm's row scale, then per head the norm / RoPE / bf16
+//          store of g4_kv_append_normrope (q to q_out, k and v to the cache);
+//   epi 1: o_proj (A = attention output rows, Bw = Wo): the post-attention
+//          RMSNorm over the N = D columns of a row (one cluster of CTAs per
+//          row block) and the residual add, out = h + norm(A Bw^T) w.
+struct GemmArgs {
+  int epi;
+  int M, N, K;
+  int* err;
+  // epi 0
+  int B, T, H, Hkv, hd, max_len, ring, n_rot;
+  float eps;       // per-head norm eps (epi 0) / post-attention norm eps (epi 1)
+  float eps_in;    // input RMSNorm eps (epi 0)
+  const float* q_w;
+  const float* k_w;
+  const int32_t* positions;  // [M]
+  void* q_out;               // [M][H][hd]
+  void* cache_k;             // [B][Hkv][max_len][hd]
+  void* cache_v;
+  float inv_freq[kMaxHalf];
+  // epi 1
+  const void* h;             // [M][N] residual
+  void* out;                 // [M][N]
+  const float* post_w;       // [N]
+};
+cudaError_t launch_gemm_tc(const GemmArgs& a, const void* A, const void* Bw, cudaStream_t s);
+
 // Decode split plan shared by the workspace query and the launch.
 // Workspace layout: ws_o, then ws_m, ws_l, tickets, each 256-byte aligned.
 // win = 1: the windowed cluster kernel (launch_decode_win), no workspace.

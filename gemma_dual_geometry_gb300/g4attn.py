@@ -59,6 +59,10 @@ SIGNATURES = {
                               _c_void_p]),
     "g4_attn_decode_noalloc": (_i32, [_P(G4LayerParams), _P(G4KVCache), _i32, _i32, _c_void_p, _c_void_p, _i32,
                                       _i32, _c_void_p, _c_void_p]),
+    "g4_qkv_project_append": (_i32, [_P(G4LayerParams), _P(G4KVCache), _i32, _i32, _c_void_p, _i32, _c_void_p,
+                                     _c_void_p, _c_void_p, _c_void_p, _i32, _i32, _c_void_p, _c_void_p]),
+    "g4_attn_out_residual": (_i32, [_c_void_p, _i32, _i32, _c_void_p, _i32, _c_void_p, ctypes.c_float, _c_void_p,
+                                    _c_void_p, _c_void_p]),
     "g4_last_error": (ctypes.c_char_p, []),
     "g4_take_device_error": (_i32, []),
 }
@@ -173,6 +177,20 @@ def g4_attn_decode_noalloc(params, caches, layer, q, seq_lens, B, max_seq_len, o
     """g4_attn_decode with the library's built-in scratch instead of a workspace."""
     _check(lib().g4_attn_decode_noalloc(ctypes.byref(params), caches, len(caches), layer, _ptr(q), _ptr(seq_lens),
                                         B, max_seq_len, _ptr(out), _stream(stream, q)))
+
+
+def g4_qkv_project_append(params, caches, layer, x, D, w_qkv, q_norm_w, k_norm_w, positions, B, T, q_out,
+                          stream=None):
+    """q/k/v projections of x (attention-norm weight folded into w_qkv) fused into the norm/RoPE/append."""
+    _check(lib().g4_qkv_project_append(ctypes.byref(params), caches, len(caches), layer, _ptr(x), int(D),
+                                       _ptr(w_qkv), _ptr(q_norm_w), _ptr(k_norm_w), _ptr(positions), B, T,
+                                       _ptr(q_out), _stream(stream, x)))
+
+
+def g4_attn_out_residual(ao, M, K, w_o, D, post_norm_w, eps, h, out, stream=None):
+    """out = h + rmsnorm(ao . w_o^T, post_norm_w, eps)."""
+    _check(lib().g4_attn_out_residual(_ptr(ao), int(M), int(K), _ptr(w_o), int(D), _ptr(post_norm_w), float(eps),
+                                      _ptr(h), _ptr(out), _stream(stream, ao)))
 
 
 def g4_last_error():

@@ -79,6 +79,19 @@ CONFIGS = {
         B=4, T=2048, H=8, Hkv=2, dtype=BF16, seed=5, encoder=True,
         types=[SLIDING, FULL], n_shared=0,
         geom={SLIDING: SLIDING_GEOM_BF16, FULL: dict(FULL_GEOM_BF16, rotary_fraction=1.0)}),
+    # The steps around the path at the stack's prefill shape (8 sequences of
+    # 4096 tokens), on a sliding and a full layer: the q / k / v projections
+    # fused into the append (model width D = 2048: the pages print no hidden
+    # size; 2048 is n_heads x the sliding head_dim), and o_proj with the
+    # post-attention norm and the residual.
+    "qkv_proj_bf16": dict(
+        B=8, T=4096, D=2048, H=8, Hkv=2, dtype=BF16, seed=6, proj="qkv",
+        types=[SLIDING, FULL], n_shared=0,
+        geom={SLIDING: SLIDING_GEOM_BF16, FULL: FULL_GEOM_BF16}),
+    "out_proj_bf16": dict(
+        B=8, T=4096, D=2048, H=8, Hkv=2, dtype=BF16, seed=7, proj="out",
+        types=[SLIDING, FULL], n_shared=0,
+        geom={SLIDING: SLIDING_GEOM_BF16, FULL: FULL_GEOM_BF16}),
     "longctx_decode_bf16": dict(
         B=4, L=131072, H=8, Hkv=2, dtype=BF16, seed=4,
         types=[FULL, SLIDING], n_shared=0,
@@ -146,6 +159,30 @@ def layer_inputs(cfg, layer, T, owns_cache, device="cpu", step=0, B=None):
         out["v"] = normal((B, T, Hkv, hd), seed_for(s, layer, 2, step), dt, device)
         out["k_norm_w"] = norm_weight(hd, seed_for(s, layer, 4))
     return out
+
+
+def projection_inputs(cfg, layer, device="cpu"):
+    """Inputs of the projection workloads: the layer input x [B*T][D] (qkv) or
+    the attention output [B*T][H*hd] and residual h [B*T][D] (out), bf16 N(0,1);
+    weights N(0,1)/sqrt(fan-in) rounded to bf16; norm weights 1 + 0.1 N(0,1)
+    (the attention-norm weight folded into the q/k/v rows in float32, then
+    rounded to bf16 once)."""
+    geo = layer_geometry(cfg, layer)
+    hd, H, Hkv, D = geo["head_dim"], cfg["H"], cfg["Hkv"], cfg["D"]
+    M = cfg["B"] * cfg["T"]
+    s = cfg["seed"]
+    if cfg["proj"] == "qkv":
+        N = (H + 2 * Hkv) * hd
+        w = normal((N, D), seed_for(s, layer, 11), F32, device) / D ** 0.5
+        a = norm_weight(D, seed_for(s, layer, 12)).to(device)
+        return dict(x=normal((M, D), seed_for(s, layer, 10), BF16, device), w=(w * a[None, :]).to(torch.bfloat16),
+                    q_norm_w=norm_weight(hd, seed_for(s, layer, 3)).to(device),
+                    k_norm_w=norm_weight(hd, seed_for(s, layer, 4)).to(device))
+    K = H * hd
+    return dict(ao=normal((M, K), seed_for(s, layer, 13), BF16, device),
+                w=(normal((D, K), seed_for(s, layer, 14), F32, device) / K ** 0.5).to(torch.bfloat16),
+                post_w=norm_weight(D, seed_for(s, layer, 15)).to(device),
+                h=normal((M, D), seed_for(s, layer, 16), BF16, device))
 
 
 def cache_rows(cfg, layer, Lmax):

@@ -265,6 +265,59 @@ g4_status g4_decode_step(const g4_layer_params* params, const g4_kv_cache* cache
                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The step before the path, fused into it: the q / k / v projections of one
+ * layer for B*T tokens, their input RMSNorm, and the per-head norm / RoPE /
+ * KV append of g4_kv_append_normrope, on the tcgen05 tensor cores
+ * (cortiq-engine g4e.rs `g4e_forward`: `rms(h, attn_norm)`, then `matvec`
+ * with wq / wk / wv, then the per-head norm, RoPE and `append`;
+ * turbospark-runtime gemma4/attn.rs writes the projections straight into the
+ * KV slot and norms / ropes them there).  bf16 only (G4_ERR_UNSUPPORTED for
+ * float32 layers).
+ *   x        [B][T][D] bf16: the layer input (residual stream), D a multiple
+ *            of 64.
+ *   w_qkv    [N][D] bf16, N = (n_heads + 2 n_kv_heads) * head_dim rows: the
+ *            rows of Wq, then Wk, then Wv (n_heads * head_dim rows, Wq only,
+ *            on a shared layer), each column k multiplied by the attention-norm
+ *            weight attn_norm_w[k] (folded in once by the caller, as
+ *            taconite-embeddinggemma2 model.rs folds RMSNorm weights into its
+ *            GEMM operands).  The kernel applies the rest of the input norm,
+ *            the row scale (mean(x^2) + eps)^-1/2 with the layer's eps.
+ *   q_norm_w, k_norm_w, positions, q_out  as g4_kv_append_normrope (k_norm_w
+ *            NULL on a shared layer).
+ * q = (x scale) Wq^T etc. accumulate in float32 from bf16 products; the
+ * per-head norm, RoPE and the bf16 rounding (to nearest even) follow in
+ * float32.  So the stored values are those of g4_kv_append_normrope on the
+ * exact projections to within one bf16 unit in the last place, where the
+ * float32 accumulation lands next to a rounding boundary.  Writes q_out and
+ * the cache rows of the tokens' positions (positions outside a linear cache
+ * are not written), nothing else.  The launch takes one 128-token x
+ * head_dim output tile per CTA.
+ */
+g4_status g4_qkv_project_append(const g4_layer_params* params, const g4_kv_cache* caches, int32_t n_layers,
+                                int32_t layer, const void* x, int32_t D, const void* w_qkv, const float* q_norm_w,
+                                const float* k_norm_w, const int32_t* positions, int32_t B, int32_t T, void* q_out,
+                                void* stream);
+
+/*
+ * The step after the path: o_proj, the post-attention RMSNorm and the
+ * residual add (cortiq-engine g4e.rs `g4e_forward`: `wo`, then the sandwich
+ * norm `rms(.., post_attn_norm)` added to the hidden state; ferrox-models
+ * gemma4_engine.rs `forward_token_on_worker`: `o_proj`, `post_attn_norm`,
+ * residual), on the tcgen05 tensor cores, bf16:
+ *   out[m][:] = h[m][:] + rmsnorm(ao[m][:] . w_o^T, post_norm_w, eps)
+ *   ao           [M][K] bf16: attention output rows (K = n_heads * head_dim,
+ *                a multiple of 64), e.g. g4_attn_prefill's out as [B*T][H*hd]
+ *   w_o          [D][K] bf16
+ *   post_norm_w  [D] float32; eps added to the mean square
+ *   h            [M][D] bf16 residual stream; out [M][D] bf16 (may equal h)
+ * D must be a multiple of 256 and at most 2048 (G4_ERR_UNSUPPORTED): the
+ * norm's row sum is formed by one thread-block cluster of D / 256 CTAs.
+ * Accumulation and the norm in float32; out rounded to nearest even.
+ */
+g4_status g4_attn_out_residual(const void* ao, int32_t M, int32_t K, const void* w_o, int32_t D,
+                               const float* post_norm_w, float eps, const void* h, void* out, void* stream);
+
+/*
  * Bytes of device scratch built into the library for g4_attn_decode_noalloc
  * (8 MiB).  Every GPU that loads the library holds this array until the
  * process exits.

@@ -271,3 +271,37 @@ def test_binding_refuses_to_run_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(G, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         G.lib()
+
+
+def test_projection_validation(L):
+    # every call here is refused before a launch, or has no rows (B*T == 0 or
+    # M == 0): the fake addresses are never dereferenced
+    tab = _table([(G.G4_SLIDING, 256, 2, 100, 2, G.G4_BF16), None])
+
+    def qkv(p=None, layer=0, x=FAKE, D=512, w=FAKE, kw=FAKE, B=2, T=4, q_out=FAKE, tab=tab):
+        return _status(G.g4_qkv_project_append, p or _params(), tab, layer, x, D, w, FAKE, kw, FAKE, B, T, q_out, 0)
+
+    assert qkv(B=0) == G.G4_OK
+    assert qkv(T=0) == G.G4_OK
+    assert qkv(D=100) == G.G4_ERR_UNSUPPORTED                       # not a multiple of 64
+    assert qkv(D=0) == G.G4_ERR_UNSUPPORTED
+    assert qkv(_params(dtype=G.G4_F32)) == G.G4_ERR_UNSUPPORTED      # tensor cores: bf16 only
+    assert qkv(x=None) == G.G4_ERR_INVALID_ARG
+    assert qkv(w=FAKE + 8) == G.G4_ERR_INVALID_ARG
+    assert qkv(kw=None) == G.G4_ERR_INVALID_ARG                     # owning layer needs k_norm_w
+    assert qkv(B=3) == G.G4_ERR_CAPACITY
+    assert qkv(_params(head_dim=512)) == G.G4_ERR_SHARE_MISMATCH
+    assert qkv(_params(kv_share_src=0), layer=1, kw=FAKE) == G.G4_ERR_INVALID_ARG   # shared: no k_norm_w
+    assert qkv(_params(kv_share_src=0), layer=1, kw=None, B=0) == G.G4_OK
+
+    def out(M=4, K=512, D=2048, eps=1e-6, ao=FAKE, w=FAKE, h=FAKE, o=FAKE):
+        return _status(G.g4_attn_out_residual, ao, M, K, w, D, FAKE, eps, h, o, 0)
+
+    assert out(M=0) == G.G4_OK
+    assert out(M=-1) == G.G4_ERR_INVALID_ARG
+    assert out(D=2304) == G.G4_ERR_UNSUPPORTED                      # row spans more than 8 CTAs
+    assert out(D=300) == G.G4_ERR_UNSUPPORTED
+    assert out(K=96) == G.G4_ERR_UNSUPPORTED
+    assert out(eps=-1.0) == G.G4_ERR_INVALID_ARG
+    assert out(h=None) == G.G4_ERR_INVALID_ARG
+    assert out(o=FAKE + 4) == G.G4_ERR_INVALID_ARG

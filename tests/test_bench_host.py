@@ -129,3 +129,14 @@ def test_oracle_baseline_pool_runs_on_several_cores():
     (step,) = res["steps"]
     assert step["t_append"] > 0 and step["t_attn"] > 0 and step["cpu_s"] > 0
     assert step["per_token_s"] == pytest.approx(step["t_append"] / 16 + step["t_attn"] / 8)
+
+
+def test_projection_workload_arithmetic():
+    # 2 M N K per launch: q/k/v rows (H + 2 Hkv) hd, o_proj K = H hd, D = 2048
+    for name, per in (("qkv_proj_bf16", lambda hd: 2.0 * 32768 * 12 * hd * 2048),
+                      ("out_proj_bf16", lambda hd: 2.0 * 32768 * 2048 * 8 * hd)):
+        cfg = W.CONFIGS[name]
+        job = bench.ProjJob.__new__(bench.ProjJob)
+        job.cfg, job.M, job.D, job.kind = cfg, cfg["B"] * cfg["T"], cfg["D"], cfg["proj"]
+        job.geo = [W.layer_geometry(cfg, l) for l in range(2)]
+        assert [job.layer_work(l) for l in range(2)] == [per(256), per(512)]

@@ -747,3 +747,21 @@ def test_normrope_composition_norm_weight_then_rotation(hd, theta, frac, dtype):
     assert not np.allclose(rope_first, ref_q, rtol=0, atol=1e-3)
     assert not np.allclose(swapped_q, ref_q, rtol=0, atol=1e-3)
     assert not np.allclose(roped_v, ref_v, rtol=0, atol=1e-3)
+
+
+def test_qkv_projection_with_the_norm_weight_folded_into_w():
+    # rms(x, a) W^T = rms(x) (W diag(a))^T: the attention-norm weight may be
+    # multiplied into the projection's columns (the form the fused projection
+    # takes), exactly in float64
+    r = rng(80)
+    D, Nq, Nk = 64, 48, 16
+    x = r.standard_normal((3, 5, D))
+    a = 1 + 0.1 * r.standard_normal(D)
+    wq, wk, wv = r.standard_normal((Nq, D)), r.standard_normal((Nk, D)), r.standard_normal((Nk, D))
+    q1, k1, v1 = O.qkv_projection(x, a, wq, wk, wv, 1e-6)
+    q2, k2, v2 = O.qkv_projection(x, None, wq * a, wk * a, wv * a, 1e-6)
+    for u, w_ in ((q1, q2), (k1, k2), (v1, v2)):
+        assert np.allclose(u, w_, rtol=1e-13, atol=1e-13)
+    # and a shared layer projects q only
+    q3, k3, v3 = O.qkv_projection(x, a, wq, None, None, 1e-6)
+    assert k3 is None and v3 is None and np.array_equal(q3, q1)
