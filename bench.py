@@ -88,6 +88,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-workload lines after the stack")
+    ap.add_argument("--min-time", type=float, default=0.6,
+                    help="seconds of timed steps each single-workload measurement runs at least (0: --steps only)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--oracle-worker", default=None, help=argparse.SUPPRESS)
     return ap.parse_args(argv)
@@ -678,7 +680,7 @@ EXTRA_WORKLOADS = ("prefill_bf16", "decode_bf16", "longctx_decode_bf16", "ring_d
                    "qkv_proj_bf16", "out_proj_bf16")
 
 
-def measure_layer_workload(name, args, dev, min_timed_s=0.6, max_steps=4000):
+def measure_layer_workload(name, args, dev, min_timed_s=None, max_steps=4000):
     """Times one of the one- or two-layer workloads on its own.
 
     Every step (append + attention of each layer, or the fused decode step) is
@@ -690,6 +692,8 @@ def measure_layer_workload(name, args, dev, min_timed_s=0.6, max_steps=4000):
     around each attention launch, and the clocks."""
     import torch
     from gemma_dual_geometry_gb300 import workloads as W
+    if min_timed_s is None:
+        min_timed_s = args.min_time
     cfg = W.CONFIGS[name]
     job = ProjJob(cfg, dev) if cfg.get("proj") else LayerJob(cfg, dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -703,7 +707,7 @@ def measure_layer_workload(name, args, dev, min_timed_s=0.6, max_steps=4000):
     c1.record()
     torch.cuda.synchronize()
     per_step = max(c0.elapsed_time(c1) * 1e-3, 1e-6)
-    steps = int(min(max_steps, max(args.steps, -(-min_timed_s // per_step))))
+    steps = int(min(max_steps, max(args.steps, -(-min_timed_s // per_step) if min_timed_s > 0 else 0)))
     job.events = {l: [] for l in range(job.n)}
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     clocks = ClockSampler(_gpu_uuid(dev))

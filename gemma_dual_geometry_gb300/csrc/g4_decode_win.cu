@@ -182,22 +182,73 @@ __global__ void __launch_bounds__(kWinThreads, (WinCfg<HD, G>::MINB))
     fence_mbar_init();
   }
   if (a.nsplit > 1) cluster_arrive_relaxed();  // waited for before the first store to a peer
-  pdl_wait();
-  pdl_trigger();
 
-  // Keys [kbeg, L) of the sequence; this CTA holds [k0, k1).
-  const int L = min(max(a.base[b], 1), a.len_cap);
-  const int kbeg = a.sliding ? max(0, L - a.window) : 0;
-  const int k0 = kbeg + split * kWinKeys;
-  const int k1 = min(L, k0 + kWinKeys);
-  const int nvalid = max(0, k1 - k0);
-  // FUSED on a layer that owns its cache: the new key is normed here, not read.
-  const bool new_key = FUSED && a.k_raw != nullptr && L - 1 >= k0 && L - 1 < k1;
-  const int ncopy = new_key ? nvalid - 1 : nvalid;
   const size_t head_base = (static_cast<size_t>(b) * a.Hkv + kvh) * a.max_len;
   const T* gk = static_cast<const T*>(a.ck) + head_base * HD;
   const T* gv = static_cast<const T*>(a.cv) + head_base * HD;
-  __syncthreads();  // barrier initialised
+  // Keys [kbeg, L) of the sequence; this CTA holds [k0, k0 + n) of them.
+  auto first_key = [&](int Lx) { return (a.sliding ? max(0, Lx - a.window) : 0) + split * kWinKeys; };
+  auto n_keys = [&](int Lx) { return max(0, min(Lx, first_key(Lx) + kWinKeys) - first_key(Lx)); };
+  // cos / sin of position p (all threads; the pairs past n_rot are the identity)
+  auto build_table = [&](int p) {
+    for (int idx = threadIdx.x; idx < HD; idx += kWinThreads) {
+      const int j = idx >> 1, part = idx & 1;
+      if (j < a.n_rot) {
+        bool to_cos;
+        const DF v = sincos_df_part(p, a.inv_freq[j], part, to_cos);
+        (to_cos ? s_cos : s_sin)[j] = v;
+      } else if (part == 0) {
+        s_cos[j] = DF{1.0f, 0.0f};
+      } else {
+        s_sin[j] = DF{0.0f, 0.0f};
+      }
+    }
+  };
+
+  // ---- while the previous kernel on the stream may still be running
+  // (programmatic dependent launch): a speculative read of the sequence's
+  // length, the L2 prefetch of the K / V rows it implies and (fused) the
+  // cos / sin table of its position.  The prefetch only warms the cache, and
+  // the table is rebuilt below unless the length read after the wait agrees,
+  // so nothing read here reaches a result.
+  const int L_spec = min(max(a.base[b], 1), a.len_cap);
+  if (threadIdx.x == 0) {
+    const int k0s = first_key(L_spec);
+    const int ns_ = n_keys(L_spec);
+    if (ns_ > 0) {
+      if (!a.ring) {
+        prefetch_l2_bulk(gk + static_cast<size_t>(k0s) * HD, static_cast<uint32_t>(ns_) * C::ROWB);
+        prefetch_l2_bulk(gv + static_cast<size_t>(k0s) * HD, static_cast<uint32_t>(ns_) * C::ROWB);
+      } else {
+        const int r0 = k0s % a.max_len;
+        const int n0 = min(ns_, a.max_len - r0);
+        prefetch_l2_bulk(gk + static_cast<size_t>(r0) * HD, static_cast<uint32_t>(n0) * C::ROWB);
+        prefetch_l2_bulk(gv + static_cast<size_t>(r0) * HD, static_cast<uint32_t>(n0) * C::ROWB);
+        if (n0 < ns_) {
+          prefetch_l2_bulk(gk, static_cast<uint32_t>(ns_ - n0) * C::ROWB);
+          prefetch_l2_bulk(gv, static_cast<uint32_t>(ns_ - n0) * C::ROWB);
+        }
+      }
+    }
+  }
+  if constexpr (FUSED) build_table(L_spec - 1);
+  pdl_wait();
+  pdl_trigger();
+
+  const int L = min(max(a.base[b], 1), a.len_cap);
+  const int k0 = first_key(L);
+  const int nvalid = n_keys(L);
+  const int k1 = k0 + nvalid;
+  // FUSED on a layer that owns its cache: the new key is normed here, not read.
+  const bool new_key = FUSED && a.k_raw != nullptr && L - 1 >= k0 && L - 1 < k1;
+  const int ncopy = new_key ? nvalid - 1 : nvalid;
+  __syncthreads();  // barrier initialised, table built
+  if constexpr (FUSED) {
+    if (L != L_spec) {  // the length changed under the speculative read: rebuild the table
+      build_table(L - 1);
+      __syncthreads();
+    }
+  }
   if (threadIdx.x == 0) {
     const uint32_t bytes = static_cast<uint32_t>(max(ncopy, 0)) * C::ROWB;
     mbar_arrive_expect_tx(smem_u32(bar), 2 * bytes);
@@ -223,7 +274,6 @@ __global__ void __launch_bounds__(kWinThreads, (WinCfg<HD, G>::MINB))
 
   // ---- the query (and the new key / value): normed rows into shared memory
   if constexpr (FUSED) {
-    const int pos = L - 1;
     const int njobs = G + (new_key ? 2 : 0);
     auto src_of = [&](int job) -> const T* {
       if (job < G) return static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.H + kvh * G + job) * HD;
@@ -241,22 +291,8 @@ __global__ void __launch_bounds__(kWinThreads, (WinCfg<HD, G>::MINB))
       }
     };
     float f[C::EL], wf[C::EL];
-    if (warp < njobs) load_job(warp, f, wf);  // loads in flight while the table is built
-    for (int idx = threadIdx.x; idx < HD; idx += kWinThreads) {
-      const int j = idx >> 1, part = idx & 1;
-      if (j < a.n_rot) {
-        bool to_cos;
-        const DF v = sincos_df_part(pos, a.inv_freq[j], part, to_cos);
-        (to_cos ? s_cos : s_sin)[j] = v;
-      } else if (part == 0) {
-        s_cos[j] = DF{1.0f, 0.0f};
-      } else {
-        s_sin[j] = DF{0.0f, 0.0f};
-      }
-    }
-    __syncthreads();
     for (int job = warp; job < njobs; job += kWinWarps) {
-      if (job != warp) load_job(job, f, wf);
+      load_job(job, f, wf);
       norm_rope_row<T, HD, C::NPC, C::PE>(f, wf, src_of(job), w_of(job), job <= G, s_cos, s_sin, a.n_rot, a.eps,
                                           lane);
       if (job < G) {
@@ -302,7 +338,7 @@ __global__ void __launch_bounds__(kWinThreads, (WinCfg<HD, G>::MINB))
     }
   bool ok = warp_wait(smem_u32(bar), 0, a.err);
   constexpr int kSh = ilog2c(C::LPK / G);
-#pragma unroll 1
+#pragma unroll
   for (int pass = 0; pass < C::NPASS; ++pass) {
     const int key = pass * C::KPP + warp * C::KPW + lane / C::LPK;
     float part_s[G];
@@ -366,13 +402,18 @@ __global__ void __launch_bounds__(kWinThreads, (WinCfg<HD, G>::MINB))
   {
     const int dp = threadIdx.x % C::NDP;
     const int ks = threadIdx.x / C::NDP;
-    float2 acc[G];
+    // every key of the slice, unrolled, two accumulator sets (even / odd
+    // keys); keys past this CTA's valid ones read nothing (their rows may
+    // hold anything, and their probabilities are zero)
+    float2 acc[2][G];
 #pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = make_float2(0.0f, 0.0f);
-    const int kend = min(nvalid, (ks + 1) * C::KPS);
-#pragma unroll 4
-    for (int key = ks * C::KPS; key < kend; ++key) {
-      const uint32_t vw = *reinterpret_cast<const uint32_t*>(sV + key * C::ROWB + dp * 4);
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+      for (int h = 0; h < G; ++h) acc[u][h] = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int kk = 0; kk < C::KPS; ++kk) {
+      const int key = ks * C::KPS + kk;
+      const uint32_t vw = key < nvalid ? *reinterpret_cast<const uint32_t*>(sV + key * C::ROWB + dp * 4) : 0u;
       const float2 vv = make_float2(bf16_lo(vw), bf16_hi(vw));
       float pk[G];
       if constexpr (G % 4 == 0) {
@@ -386,12 +427,15 @@ __global__ void __launch_bounds__(kWinThreads, (WinCfg<HD, G>::MINB))
         for (int h = 0; h < G; ++h) pk[h] = s_p[key * G + h];
       }
 #pragma unroll
-      for (int h = 0; h < G; ++h) acc[h] = fma2w(make_float2(pk[h], pk[h]), vv, acc[h]);
+      for (int h = 0; h < G; ++h) acc[kk & 1][h] = fma2w(make_float2(pk[h], pk[h]), vv, acc[kk & 1][h]);
     }
+    float2 accs[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) accs[h] = make_float2(acc[0][h].x + acc[1][h].x, acc[0][h].y + acc[1][h].y);
     __syncthreads();  // every K / V read is done: the area takes the slice sums
     float2* red = reinterpret_cast<float2*>(smem);  // [NKS][G][HD/2]
 #pragma unroll
-    for (int h = 0; h < G; ++h) red[(ks * G + h) * C::NDP + dp] = acc[h];
+    for (int h = 0; h < G; ++h) red[(ks * G + h) * C::NDP + dp] = accs[h];
   }
   __syncthreads();
   // The slice sums: this CTA's unnormalised output.  With one CTA it is
@@ -427,20 +471,27 @@ __global__ void __launch_bounds__(kWinThreads, (WinCfg<HD, G>::MINB))
       const float* ro = reinterpret_cast<const float*>(smem + C::RO_OFF);
       const float* rm = reinterpret_cast<const float*>(smem + C::RM_OFF);
       const float* rl = reinterpret_cast<const float*>(smem + C::RL_OFF);
-      for (int idx = threadIdx.x; idx < G * HD; idx += kWinThreads) {
-        const int h = idx / HD;
+      // log-sum-exp weight of each (split, head), normalised: once per head
+      float* wts = s_sc;  // [ns][G] (the scores are no longer needed)
+      if (threadIdx.x < G) {
+        const int h = threadIdx.x;
         float M = -INFINITY;
         for (int r = 0; r < ns; ++r) M = fmaxf(M, rm[r * G + h]);
-        float num = 0.0f, den = 0.0f;
+        float den = 0.0f;
         for (int r = 0; r < ns; ++r) {
           const float mr = rm[r * G + h];
-          if (mr != -INFINITY) {
-            const float w = ex2_approx(mr - M);
-            num = fmaf(w, ro[r * G * HD + idx], num);
-            den = fmaf(w, rl[r * G + h], den);
-          }
+          const float w = mr == -INFINITY ? 0.0f : ex2_approx(mr - M);
+          wts[r * G + h] = w;
+          den = fmaf(w, rl[r * G + h], den);
         }
-        const float val = den > 0.0f ? num / den : 0.0f;
+        const float inv = den > 0.0f ? 1.0f / den : 0.0f;
+        for (int r = 0; r < ns; ++r) wts[r * G + h] *= inv;
+      }
+      __syncthreads();
+      for (int idx = threadIdx.x; idx < G * HD; idx += kWinThreads) {
+        const int h = idx / HD;
+        float val = 0.0f;
+        for (int r = 0; r < ns; ++r) val = fmaf(wts[r * G + h], ro[r * G * HD + idx], val);
         store_elems<1>(out + idx, &val);
       }
     }

@@ -266,6 +266,13 @@ __device__ __forceinline__ void tma_store_5d(const CUtensorMap* map, uint32_t sr
       : "memory");
 }
 
+// Hint: bring [src, src + bytes) into L2 (bytes a multiple of 16).  A
+// prefetch only moves lines into the cache; a later load still reads the
+// current contents, so it may be issued before the data is final.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Waits until the bulk stores committed so far have finished reading their
