@@ -231,7 +231,25 @@ __global__ void __launch_bounds__(kWinThreads, (WinCfg<HD, G>::MINB))
       }
     }
   }
-  if constexpr (FUSED) build_table(L_spec - 1);
+  if constexpr (FUSED) {
+    // the rows the norm reads: the G raw q rows, the new k and v rows, the
+    // weights (one 16-byte-multiple prefetch each, by otherwise idle lanes)
+    if (warp == kWinWarps - 1 && lane < G + 4) {
+      const void* src = nullptr;
+      uint32_t bytes = C::ROWB;
+      if (lane < G) {
+        src = static_cast<const T*>(a.q) + (static_cast<size_t>(b) * a.H + kvh * G + lane) * HD;
+      } else if (lane < G + 2) {
+        const void* raw = lane == G ? a.k_raw : a.v_raw;
+        if (raw != nullptr) src = static_cast<const T*>(raw) + (static_cast<size_t>(b) * a.Hkv + kvh) * HD;
+      } else {
+        src = lane == G + 2 ? static_cast<const void*>(a.q_w) : static_cast<const void*>(a.k_w);
+        bytes = HD * 4;
+      }
+      if (src != nullptr) prefetch_l2_bulk(src, bytes);
+    }
+    build_table(L_spec - 1);
+  }
   pdl_wait();
   pdl_trigger();
 

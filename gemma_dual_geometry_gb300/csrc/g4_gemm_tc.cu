@@ -61,7 +61,7 @@ struct GemmCfg {
   static constexpr int A_B = kGM * kGK * 2;               // 16 KB
   static constexpr int B_B = BN * kGK * 2;                // BN x 128 B
   static constexpr int STAGE_B = A_B + B_B;
-  static constexpr int BAR_B = 1024;
+  static constexpr int BAR_B = 4096;  // barriers (1 KB), then the epilogue's weight row (<= 512 floats)
   // Tiles of up to 256 columns run two CTAs per SM (TMEM: 2 x 256 columns),
   // so one CTA's epilogue overlaps the other's main loop; 512 columns fill
   // TMEM and take the SM alone.
@@ -88,6 +88,9 @@ struct GemmBars {
   float red[kGM];  // epi 1: this CTA's per-row sums of squares (read by the cluster)
 };
 static_assert(sizeof(GemmBars) <= 1024, "barrier block");
+
+// The 128 epilogue threads meet (named barrier 1).
+__device__ __forceinline__ void epilogue_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -235,6 +238,21 @@ __global__ void __launch_bounds__(kGThreads, (GemmCfg<BN>::CTAS_PER_SM))
     const int m = quarter * 32 + lane;  // tile row == TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     bool ok = aligned;
+    // this tile's weight row into shared memory (read by every thread per
+    // column): the head's q_norm / k_norm weight (epi 0; none on v heads),
+    // the post-attention norm weight of the tile's columns (epi 1)
+    {
+      float* s_w = reinterpret_cast<float*>(smem + C::BAR_OFF + 1024);
+      const float* wsrc = nullptr;
+      if constexpr (EPI == 0) {
+        wsrc = n_tile < a.H ? a.q_w : (n_tile < a.H + a.Hkv ? a.k_w : nullptr);
+      } else {
+        wsrc = a.post_w + n0;
+      }
+      const int t = threadIdx.x - 64;
+      for (int i = t; i < BN; i += 128) s_w[i] = wsrc != nullptr ? wsrc[i] : 1.0f;
+      epilogue_sync();
+    }
     if constexpr (EPI == 0) {
       // the input RMSNorm's sum of squares of row m, from the A tiles in flight
       for (int k = 0; k < nk && ok; ++k) {
@@ -269,7 +287,7 @@ __global__ void __launch_bounds__(kGThreads, (GemmCfg<BN>::CTAS_PER_SM))
         const int hd = BN;
         const int hn = n_tile;  // head: q heads, then k heads, then v heads
         const int kind = hn < a.H ? 0 : (hn < a.H + a.Hkv ? 1 : 2);
-        const float* w = kind == 0 ? a.q_w : (kind == 1 ? a.k_w : nullptr);
+        const float* s_w = reinterpret_cast<const float*>(smem + C::BAR_OFF + 1024);  // ones on v heads
         const bool rope = kind < 2;
         // input norm row scale, then this head's sum of squares of acc
         const float rx = __frsqrt_rn(fmaf(row_sq, 1.0f / static_cast<float>(a.K), a.eps_in));
@@ -313,12 +331,8 @@ __global__ void __launch_bounds__(kGThreads, (GemmCfg<BN>::CTAS_PER_SM))
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int j = c * 32 + i + e;
-              float ya = __uint_as_float(lo[i + e]) * scale;
-              float yb = __uint_as_float(hi[i + e]) * scale;
-              if (w != nullptr) {
-                ya *= w[j];
-                yb *= w[j + BN / 2];
-              }
+              const float ya = __uint_as_float(lo[i + e]) * scale * s_w[j];
+              const float yb = __uint_as_float(hi[i + e]) * scale * s_w[j + BN / 2];
               if (rope && j < a.n_rot) {
                 float cj, sj;
                 rope_cos_sin(pos, a.inv_freq[j], cj, sj);
@@ -374,34 +388,44 @@ __global__ void __launch_bounds__(kGThreads, (GemmCfg<BN>::CTAS_PER_SM))
       const float rn = __frsqrt_rn(fmaf(tot, 1.0f / static_cast<float>(a.N), a.eps));
       const bool live = *abort == 0;
       if (live) {
+        const float* s_w = reinterpret_cast<const float*>(smem + C::BAR_OFF + 1024);
+        const bool rv = gm < a.M;
+        const uint4* hrow = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.h) +
+                                                           static_cast<size_t>(rv ? gm : 0) * a.N + n0);
+        uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                                               static_cast<size_t>(rv ? gm : 0) * a.N + n0);
+        // the residual's 32-column pieces, one piece ahead of the columns in use
+        uint4 hcur[4], hnext[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) hcur[q] = rv ? hrow[q] : make_uint4(0, 0, 0, 0);
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
+          if (c + 1 < BN / 32) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) hnext[q] = rv ? hrow[(c + 1) * 4 + q] : make_uint4(0, 0, 0, 0);
+          }
           uint32_t r[32];
           tmem_ld32(tmem + lane_off + c * 32, r);
           tc_wait_ld();
-          if (gm < a.M) {
-            const int col0 = n0 + c * 32;
-            const uint4* hp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.h) +
-                                                             static_cast<size_t>(gm) * a.N + col0);
-            uint4 hv[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) hv[q] = hp[q];
+          if (rv) {
             uint32_t ov[16];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const uint32_t hw[4] = {hv[q].x, hv[q].y, hv[q].z, hv[q].w};
+              const uint32_t hw[4] = {hcur[q].x, hcur[q].y, hcur[q].z, hcur[q].w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
                 const int i = q * 8 + e * 2;
-                const float y0 = fmaf(__uint_as_float(r[i]) * rn, a.post_w[col0 + i], bf16_lo(hw[e]));
-                const float y1 = fmaf(__uint_as_float(r[i + 1]) * rn, a.post_w[col0 + i + 1], bf16_hi(hw[e]));
+                const float y0 = fmaf(__uint_as_float(r[i]) * rn, s_w[c * 32 + i], bf16_lo(hw[e]));
+                const float y1 = fmaf(__uint_as_float(r[i + 1]) * rn, s_w[c * 32 + i + 1], bf16_hi(hw[e]));
                 ov[q * 4 + e] = pack_bf16x2(y0, y1);
               }
             }
-            uint4* op = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + static_cast<size_t>(gm) * a.N + col0);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) op[q] = make_uint4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
+            for (int q = 0; q < 4; ++q)
+              orow[c * 4 + q] = make_uint4(ov[4 * q], ov[4 * q + 1], ov[4 * q + 2], ov[4 * q + 3]);
           }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) hcur[q] = hnext[q];
         }
       }
     }
