@@ -45,18 +45,30 @@ METRIC = "prefill attn tokens/s and decode KV GB/s vs GB300 roofline, 1 GPU"
 WORKLOAD = "stack42_bf16"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DECODE_EVENT_STEPS = (0, 32, 64, 96, 127)
-# DRAM bytes (read + write) per launch from one ncu capture of each kernel on
-# the 42-layer stack with an 8-step decode phase (dram__bytes.sum.per_second x
-# gpu__time_duration); the decode figures are for the first decode step.
-# Each figure carries the kernel's source files and the first 16 hex digits
-# of their SHA-256 when it was captured: once the sources differ, the
+# DRAM bytes (read + write) per launch from the ncu launch lists in
+# profiles/ (dram__bytes_read.sum + dram__bytes_write.sum of each launch): the
+# stack's kernels captured on the same stack at batch 2 (stack42_bf16_b2) and
+# scaled by 4 to the benchmark's 8 sequences (every launch's bytes grow with
+# the sequences it processes), the projections captured at the benchmark's
+# own size.  Each figure carries the kernel's source files and the first 16
+# hex digits of their SHA-256 at the capture: once the sources differ, the
 # counters describe another kernel and the figure is not reported.
 PREFILL_SOURCES = ("g4_prefill_tc.cu", "g4_device.cuh", "g4_internal.h")
 DECODE_SOURCES = ("g4_attn_simt.cu", "g4_device.cuh", "g4_internal.h", "g4_normrope.cuh")
+WIN_SOURCES = ("g4_decode_win.cu", "g4_device.cuh", "g4_internal.h", "g4_normrope.cuh")
+GEMM_SOURCES = ("g4_gemm_tc.cu", "g4_device.cuh", "g4_internal.h", "g4_normrope.cuh")
 PROFILED_TRAFFIC = {
-    "prefill_full": (637334783, PREFILL_SOURCES, "d1613f02eca7b99f"),
-    "decode_full": (137716979, DECODE_SOURCES, "dfacc6f82f285597"),
-    "decode_sliding": (8492032, DECODE_SOURCES, "dfacc6f82f285597"),
+    # key: (bytes per launch, sources, digest, where it comes from)
+    "prefill_full": (523422647, PREFILL_SOURCES, "0d43a4695d5c39a2",
+                     "ncu launch list, 42-layer stack at batch 2, layer-5 launches, x 4 sequences"),
+    "decode_full": (134668971, DECODE_SOURCES, "1b8aa93a5cd45d12",
+                    "ncu launch list, 42-layer stack at batch 2, full-layer decode steps, x 4 sequences"),
+    "decode_sliding": (8708935, WIN_SOURCES, "9639212a168ccbe2",
+                       "ncu launch list, 42-layer stack at batch 2, sliding-layer decode steps, x 4 sequences"),
+    "qkv_sliding": (299654810, GEMM_SOURCES, "9df637440ee7ed53", "ncu launch list, qkv_proj_bf16, sliding layer"),
+    "qkv_full": (513048166, GEMM_SOURCES, "9df637440ee7ed53", "ncu launch list, qkv_proj_bf16, full layer"),
+    "out_sliding": (378696346, GEMM_SOURCES, "9df637440ee7ed53", "ncu launch list, out_proj_bf16, sliding layer"),
+    "out_full": (584917094, GEMM_SOURCES, "9df637440ee7ed53", "ncu launch list, out_proj_bf16, full layer"),
 }
 
 
@@ -70,9 +82,11 @@ def kernel_sources_hash(files):
     return m.hexdigest()[:16]
 
 
-def profiled_traffic(key, source):
+def profiled_traffic(key):
     """(traffic per launch or None, where it comes from)."""
-    nbytes, files, digest = PROFILED_TRAFFIC[key]
+    if key not in PROFILED_TRAFFIC:
+        return None, "no capture of this kernel"
+    nbytes, files, digest, source = PROFILED_TRAFFIC[key]
     if kernel_sources_hash(files) != digest:
         return None, source + "; not reported: the kernel's sources changed after that capture"
     return nbytes, source
@@ -447,15 +461,15 @@ def run_ours(args, cfg):
                       peak_kind=f"{peak_src} bf16 dense, sustained (timed inside a long step)",
                       flops_per_launch=pf_flops, avg_launch_ms=pf_avg * 1e3, launches_sampled=len(pf_launch),
                       launches_per_step=len(job.full_layers))
-    rl_prefill["traffic"], rl_prefill["traffic_source"] = profiled_traffic(
-        "prefill_full", "ncu capture, 42-layer stack, layer 5")
+    rl_prefill["traffic"], rl_prefill["traffic_source"] = profiled_traffic("prefill_full")
     rl_prefill["frac"] = rl_prefill["achieved"] / rl_prefill["peak"]
     rl_prefill["frac_of_burst"] = rl_prefill["achieved"] / peaks["bf16_tflops"]
     rooflines = [rl_prefill]
     kinds = (("full", job.full_layers, "attn_simt_kernel<bf16,512,4,fused> (full-layer decode step: append + "
                                        "split-KV attention + last-CTA merge)"),
-             ("sliding", job.sliding_layers, "attn_simt_kernel<bf16,256,4,fused> (sliding-layer decode step, "
-                                             "window 512: append + split-KV attention + last-CTA merge)"))
+             ("sliding", job.sliding_layers, "decode_win_kernel<256,4,fused> (sliding-layer decode step, window "
+                                             "512: append + a cluster of eight 64-key CTAs merged in the leader's "
+                                             "shared memory)"))
     for kind, layers, name in kinds:
         samples = [(s, l, t) for (s, l, t, _) in dec_samples if l in layers]
         n_launches = sum(n for (_, l, _, n) in dec_samples if l in layers)
@@ -470,14 +484,13 @@ def run_ours(args, cfg):
                       avg_launch_ms=avg_t * 1e3, launches_sampled=n_launches,
                       launches_per_step=len(layers) * cfg["decode_steps"],
                       per_launch_gbs_min=min(per) / 1e9, per_launch_gbs_max=max(per) / 1e9)
-        rl_dec["traffic"], rl_dec["traffic_source"] = profiled_traffic(
-            "decode_" + kind,
-            f"ncu capture, 42-layer stack, layer {'5' if kind == 'full' else '0'}, first decode step")
+        rl_dec["traffic"], rl_dec["traffic_source"] = profiled_traffic("decode_" + kind)
         rl_dec["frac"] = rl_dec["achieved"] / rl_dec["peak"]
         if kind == "sliding":
-            rl_dec["note"] = ("latency-bound: %.1f MB per launch, so the launch and the kernel's dependent "
-                              "phases (norm, split merge) outweigh the streaming; timed over runs of 5 "
-                              "consecutive sliding layers (one event pair per run)" % (avg_b / 1e6))
+            rl_dec["note"] = ("latency-bound: %.1f MB per launch, so the kernel's chain of dependent phases "
+                              "(cos/sin table, norm, scores, softmax, P.V, cluster merge) outweighs the "
+                              "streaming; timed over runs of 5 consecutive sliding layers (one event pair per "
+                              "run)" % (avg_b / 1e6))
         rooflines.append(rl_dec)
     # the dominant kernel is the one with the most time per step
     dominant = max(rooflines, key=lambda r: r["avg_launch_ms"] * r["launches_per_step"])
@@ -745,6 +758,8 @@ def measure_layer_workload(name, args, dev, min_timed_s=None, max_steps=4000):
                      frac_of_sustained=ach / peaks["bf16_tflops_sustained"], flops_per_launch=w,
                      peak_kind=f"{src} bf16 dense, burst (kernel timed alone; frac_of_sustained against the "
                                f"sustained peak)")
+        if isinstance(job, ProjJob):
+            r["traffic"], r["traffic_source"] = profiled_traffic(f"{job.kind}_{r['layer_type']}")
         per_layer.append(r)
     if job.decode:
         step_bytes = sum(job.layer_work(l) for l in range(job.n))

@@ -69,13 +69,14 @@ def test_ring_workload_builds_ring_caches_on_the_host():
 def test_profiled_traffic_only_for_the_captured_kernel_source(monkeypatch):
     # a figure is reported while the kernel's sources hash to the digest taken
     # at the capture, and withheld (None) once they differ
-    files = bench.DECODE_SOURCES
+    files = bench.WIN_SOURCES
     now = bench.kernel_sources_hash(files)
-    monkeypatch.setitem(bench.PROFILED_TRAFFIC, "decode_sliding", (123, files, now))
-    assert bench.profiled_traffic("decode_sliding", "capture") == (123, "capture")
-    monkeypatch.setitem(bench.PROFILED_TRAFFIC, "decode_sliding", (123, files, "0" * 16))
-    t, src = bench.profiled_traffic("decode_sliding", "capture")
+    monkeypatch.setitem(bench.PROFILED_TRAFFIC, "decode_sliding", (123, files, now, "capture"))
+    assert bench.profiled_traffic("decode_sliding") == (123, "capture")
+    monkeypatch.setitem(bench.PROFILED_TRAFFIC, "decode_sliding", (123, files, "0" * 16, "capture"))
+    t, src = bench.profiled_traffic("decode_sliding")
     assert t is None and "changed" in src
+    assert bench.profiled_traffic("no_such_kernel")[0] is None
 
 
 def _free_port():
