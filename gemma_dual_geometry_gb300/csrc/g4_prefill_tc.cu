@@ -29,8 +29,9 @@
 //               boxes, one request per 32-64 KB (a request costs the SM about
 //               the same whatever its size), through a ring of slots,
 //               128-byte swizzled.
-//   warp 1      allocates TMEM; one lane issues every tcgen05.mma from
-//               precomputed descriptors:
+//   warp 1      allocates TMEM and runs the MMA issue loop converged; one
+//               elected lane issues every tcgen05.mma from precomputed
+//               descriptors:
 //                 S[j%2] = Q K_j^T      (M=128, N=128, K=head_dim; A, B from
 //                                        shared memory, K-major)
 //                 O     += P_j V_j      (M=128, N=DV,  K=128; A = P_j from
@@ -349,23 +350,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // One lane waits and issues (tcgen05.mma is issued by a single thread;
-    // waiting with the whole warp only adds latency between MMAs).  Tile
-    // parities run on across items (J counts every tile of the CTA).
-    if (lane == 0) {
+    // The whole warp runs the issue loop converged (waits included) and one
+    // elected lane issues each tcgen05.mma and commit: the loop's descriptor
+    // and ring arithmetic stays warp-uniform, and issue keeps ahead of the
+    // tensor pipe (run by one lane inside a lane test, the loop issued each
+    // MMA slower than the pipe executes it).  Tile parities run on across
+    // items (J counts every tile of the CTA).
+    {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBM, kBN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBM, C::DV, 0, 1);
       bool ok = true;
       // Descriptors are built once; a slot, a 64-dim chunk or a 16-element
       // K step only moves the start address (16-byte units in the low bits,
       // which stay below 2^14 for any shared-memory address).  Building them
-      // per instruction costs the issuing thread more cycles than the MMA.
+      // per instruction costs the issue loop more cycles than the MMA.
       const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
       const uint64_t dk0 = smem_desc_sw128(sRing, 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(sRing, C::VKP * 128, 1024);
-      // Ring state, advanced incrementally: the issuing thread's own
-      // instruction latency sits between MMAs of 64 cycles, so there is no
-      // division, modulo or multiply on this path.
+      // Ring state, advanced incrementally: the issue loop's own instruction
+      // latency sits between MMAs of 64 cycles, so there is no division,
+      // modulo or multiply on this path.
       int slot = 0;        // ring slot of the next part
       uint32_t phase = 0;  // parity of that slot's current use
       uint32_t soff = 0;   // slot * SLOTB in descriptor units (16 bytes)
@@ -380,20 +384,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto release = [&]() {
-        tc_commit(empty0 + slot * 8);
+        tc_commit_elect(empty0 + slot * 8);
         advance();
       };
       int J = 0;   // tiles of earlier items
       int nq = 0;  // items started
       for (int n = 0; ok; ++n) {
         const int e = n & 3;
-        if (!thread_wait(smem_u32(&bars->it_full[e]), (n >> 2) & 1, a.err, abort)) break;
+        if (!warp_wait(smem_u32(&bars->it_full[e]), (n >> 2) & 1, a.err, abort)) break;
         const int it = *reinterpret_cast<volatile int*>(&bars->items[e]);
-        mbar_arrive(smem_u32(&bars->it_empty[e]));
+        if (lane == 0) mbar_arrive(smem_u32(&bars->it_empty[e]));
+        __syncwarp();
         if (it < 0) break;
         const TcItem w = tc_item<C::NDH, BIDIR>(a, it, nqt);
         if (w.ntiles == 0) continue;
-        if (!thread_wait(smem_u32(&bars->q_full), nq & 1, a.err, abort)) break;
+        if (!warp_wait(smem_u32(&bars->q_full), nq & 1, a.err, abort)) break;
         ++nq;
         tc_fence_after();
         auto mma_qk = [&](int j) {
@@ -402,34 +407,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint64_t ad = dq0;
 #pragma unroll 1
           for (int p2 = 0; p2 < C::KPARTS; ++p2) {
-            if (!thread_wait(full0 + slot * 8, phase, a.err, abort)) { ok = false; return; }
+            if (!warp_wait(full0 + slot * 8, phase, a.err, abort)) { ok = false; return; }
             tc_fence_after();
             uint64_t bd = dk0 + soff;
 #pragma unroll
             for (int c = 0; c < C::CPP; ++c) {
-              tc_mma_ss(dS, ad, bd, idesc_qk, (p2 > 0 || c > 0) ? 1u : 0u);
-              tc_mma_ss(dS, ad + 2, bd + 2, idesc_qk, 1u);
-              tc_mma_ss(dS, ad + 4, bd + 4, idesc_qk, 1u);
-              tc_mma_ss(dS, ad + 6, bd + 6, idesc_qk, 1u);
+              tc_mma_ss_elect(dS, ad, bd, idesc_qk, (p2 > 0 || c > 0) ? 1u : 0u);
+              tc_mma_ss_elect(dS, ad + 2, bd + 2, idesc_qk, 1u);
+              tc_mma_ss_elect(dS, ad + 4, bd + 4, idesc_qk, 1u);
+              tc_mma_ss_elect(dS, ad + 6, bd + 6, idesc_qk, 1u);
               ad += kChunkB >> 4;
               bd += kChunkB >> 4;
             }
             release();
           }
-          tc_commit(smem_u32(&bars->s_full[sb]));
+          tc_commit_elect(smem_u32(&bars->s_full[sb]));
           // after the item's last QK, the Q area may take the next item's Q
-          if (j == w.ntiles - 1) tc_commit(smem_u32(&bars->q_free));
+          if (j == w.ntiles - 1) tc_commit_elect(smem_u32(&bars->q_free));
         };
         auto mma_pv = [&](int j) {
           const int sb = (J + j) & 1;
-          if (!thread_wait(smem_u32(&bars->p_full[sb]), ((J + j) >> 1) & 1, a.err, abort)) { ok = false; return; }
+          if (!warp_wait(smem_u32(&bars->p_full[sb]), ((J + j) >> 1) & 1, a.err, abort)) { ok = false; return; }
           tc_fence_after();
           const int kt = w.kt_begin + j;
           uint32_t ta = tmem + sb * kBN;  // P_j: 128 keys as 64 packed columns
           const bool last = j == w.ntiles - 1;
 #pragma unroll 1
           for (int p2 = 0; p2 < C::VPARTS; ++p2) {
-            if (!thread_wait(full0 + slot * 8, phase, a.err, abort)) { ok = false; return; }
+            if (!warp_wait(full0 + slot * 8, phase, a.err, abort)) { ok = false; return; }
             // Rows of keys past the cache's filled length may hold anything
             // (even NaN, and 0 * NaN = NaN); zero them before they meet P
             // (only in the part holding the end of the keys).
@@ -438,19 +443,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int nvalid = max(0, w.Lk - key0);
               uint8_t* slot_ptr = smem + C::RING_OFF + slot * C::SLOTB;
               const int nbad = C::VKP - nvalid;
-              for (int i = 0; i < (C::DV / 64) * nbad * 8; ++i) {
+              for (int i = lane; i < (C::DV / 64) * nbad * 8; i += 32) {
                 const int dc = i / (nbad * 8);
                 const int rr = (i / 8) % nbad + nvalid;
                 const int pc = i % 8;
                 *reinterpret_cast<uint4*>(slot_ptr + dc * C::VKP * 128 + rr * 128 + pc * 16) = make_uint4(0, 0, 0, 0);
               }
               fence_proxy_async_smem();
+              __syncwarp();
             }
             tc_fence_after();
             const uint64_t bd = dv0 + soff;
 #pragma unroll
             for (int kk = 0; kk < C::VKP / 16; ++kk)
-              tc_mma_ts(tmem_O, ta + kk * 8, bd + static_cast<uint64_t>(kk * 128), idesc_pv,
+              tc_mma_ts_elect(tmem_O, ta + kk * 8, bd + static_cast<uint64_t>(kk * 128), idesc_pv,
                         (j > 0 || p2 > 0 || kk > 0) ? 1u : 0u);
             ta += C::VKP / 2;
             // The item's last OSLOTS V parts stay held: the epilogue stages
@@ -460,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               release();
           }
-          tc_commit(smem_u32(&bars->o_done[sb]));
+          tc_commit_elect(smem_u32(&bars->o_done[sb]));
         };
         mma_qk(0);
         for (int j = 0; j < w.ntiles && ok; ++j) {
@@ -470,8 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         J += w.ntiles;
       }
       // Every MMA issued so far completes before TMEM is released.
-      tc_commit(smem_u32(&bars->drain));
-      thread_wait(smem_u32(&bars->drain), 0, nullptr);
+      tc_commit_elect(smem_u32(&bars->drain));
+      warp_wait(smem_u32(&bars->drain), 0, nullptr);
     }
     __syncwarp();
   } else {
