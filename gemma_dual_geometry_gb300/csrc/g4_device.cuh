@@ -334,6 +334,19 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
+// One lane of a converged warp (the lowest active one) is told true.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, e;\n\t}"
+      : "=r"(r)
+      :
+      : "memory");
+  return r != 0;
+}
+
 // The same three issued from a converged warp: elect.sync picks one lane (the
 // lowest active one, so always the same lane and one thread's issue order)
 // and only it issues.  A warp that runs its issue loop converged keeps the

@@ -183,35 +183,46 @@ __global__ void __launch_bounds__(kGThreads, (GemmCfg<BN>::CTAS_PER_SM))
   float row_sq = 0.0f;  // epilogue thread: its row's sum of squares (of A in epi 0, of the tile in epi 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && aligned) {
-      prefetch_tensormap(&tm_a);
-      prefetch_tensormap(&tm_b);
+    // The warp runs the loop converged; one elected lane posts each stage's
+    // byte count and issues its copies.
+    if (aligned) {
+      if (elect_one()) {
+        prefetch_tensormap(&tm_a);
+        prefetch_tensormap(&tm_b);
+      }
+      __syncwarp();
       int issued = 0;
       for (int k = 0; k < nk; ++k) {
         const int s = k % C::NSTAGE;
         const uint32_t ph = (k / C::NSTAGE) & 1;
-        if (k >= C::NSTAGE && !thread_wait(smem_u32(&bars->empty[s]), ph ^ 1u, a.err, abort)) break;
+        if (k >= C::NSTAGE && !warp_wait(smem_u32(&bars->empty[s]), ph ^ 1u, a.err, abort)) break;
         const uint32_t fb = smem_u32(&bars->full[s]);
-        mbar_arrive_expect_tx(fb, C::STAGE_B);
-        tma_load_2d(sA(s), &tm_a, k * kGK, m0, fb);
+        if (elect_one()) {
+          mbar_arrive_expect_tx(fb, C::STAGE_B);
+          tma_load_2d(sA(s), &tm_a, k * kGK, m0, fb);
 #pragma unroll
-        for (int bx = 0; bx < C::NBOX; ++bx)
-          tma_load_2d(sB(s) + bx * C::MMA_N * 128, &tm_b, k * kGK, n0 + bx * C::MMA_N, fb);
+          for (int bx = 0; bx < C::NBOX; ++bx)
+            tma_load_2d(sB(s) + bx * C::MMA_N * 128, &tm_b, k * kGK, n0 + bx * C::MMA_N, fb);
+        }
+        __syncwarp();
         issued = k + 1;
       }
       // copies still in flight must land before the CTA may exit
       for (int k = issued > C::NSTAGE ? issued - C::NSTAGE : 0; k < issued; ++k)
-        thread_wait(smem_u32(&bars->full[k % C::NSTAGE]), (k / C::NSTAGE) & 1, nullptr);
+        warp_wait(smem_u32(&bars->full[k % C::NSTAGE]), (k / C::NSTAGE) & 1, nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0 && aligned) {
+    // The warp runs the loop converged and one elected lane issues each MMA
+    // and commit (run by one lane inside a lane test, the loop issued MMAs
+    // slower than the tensor pipe executes them).
+    if (aligned) {
       constexpr uint32_t idesc = idesc_bf16_f32(kGM, C::MMA_N, 0, 0);
       bool ok = true;
       for (int k = 0; k < nk && ok; ++k) {
         const int s = k % C::NSTAGE;
-        if (!thread_wait(smem_u32(&bars->full[s]), (k / C::NSTAGE) & 1, a.err, abort)) {
+        if (!warp_wait(smem_u32(&bars->full[s]), (k / C::NSTAGE) & 1, a.err, abort)) {
           ok = false;
           break;
         }
@@ -222,14 +233,14 @@ __global__ void __launch_bounds__(kGThreads, (GemmCfg<BN>::CTAS_PER_SM))
         for (int kk = 0; kk < kGK / 16; ++kk)
 #pragma unroll
           for (int nm = 0; nm < C::NMMA; ++nm)
-            tc_mma_ss(tmem + nm * C::MMA_N, ad + 2 * kk, bd + 2 * kk + nm * ((C::MMA_N * 128) >> 4), idesc,
-                      (k > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(smem_u32(&bars->empty[s]));
+            tc_mma_ss_elect(tmem + nm * C::MMA_N, ad + 2 * kk, bd + 2 * kk + nm * ((C::MMA_N * 128) >> 4), idesc,
+                            (k > 0 || kk > 0) ? 1u : 0u);
+        tc_commit_elect(smem_u32(&bars->empty[s]));
       }
       // acc_full: every MMA issued has completed (also on the way out after
       // an abort, so TMEM is not released under a running MMA)
-      tc_commit(smem_u32(&bars->acc_full));
-      thread_wait(smem_u32(&bars->acc_full), 0, nullptr);
+      tc_commit_elect(smem_u32(&bars->acc_full));
+      warp_wait(smem_u32(&bars->acc_full), 0, nullptr);
     }
     __syncwarp();
   } else {

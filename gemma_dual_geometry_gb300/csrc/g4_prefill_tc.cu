@@ -24,11 +24,11 @@
 // them on through a 4-entry queue in shared memory), with its barriers, ring and TMEM
 // running on from item to item, so the next item's Q and first K parts load
 // while the current one finishes.  Warp roles (320 threads):
-//   warp 0      TMA producer (one lane): the Q tile, then K parts (128 keys x
-//               64..256 dims) and V parts (64..128 keys x DV dims) as 5-D
-//               boxes, one request per 32-64 KB (a request costs the SM about
-//               the same whatever its size), through a ring of slots,
-//               128-byte swizzled.
+//   warp 0      TMA producer (converged; one elected lane issues): the Q
+//               tile, then K parts (128 keys x 64..256 dims) and V parts
+//               (64..128 keys x DV dims) as 5-D boxes, one request per
+//               32-64 KB (a request costs the SM about the same whatever its
+//               size), through a ring of slots, 128-byte swizzled.
 //   warp 1      allocates TMEM and runs the MMA issue loop converged; one
 //               elected lane issues every tcgen05.mma from precomputed
 //               descriptors:
@@ -270,15 +270,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // One lane issues every copy (a warp-wide wait per slot would cost more
-    // than the copy takes to issue).  The ring runs on across work items: the
-    // next item's Q is loaded once the last QK MMA of the current one has
-    // read the old Q, and its first K parts go into whatever slots are free
-    // while the current item finishes.
-    if (lane == 0) {
-      prefetch_tensormap(&tm_q);
-      prefetch_tensormap(&tm_k);
-      prefetch_tensormap(&tm_v);
+    // The warp runs the loop converged; one elected lane draws the work items
+    // and issues every copy.  The ring runs on across work items: the next
+    // item's Q is loaded once the last QK MMA of the current one has read the
+    // old Q, and its first K parts go into whatever slots are free while the
+    // current item finishes.
+    {
+      if (elect_one()) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+      }
+      __syncwarp();
       const uint32_t qb = smem_u32(&bars->q_full);
       bool ok = true;
       int seq = 0;
@@ -295,21 +298,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int n = 0; ok; ++n) {
         // next work item into queue entry n % 4 (once both readers are done with its last use)
         const int e = n & 3;
-        if (n >= 4 && !thread_wait(smem_u32(&bars->it_empty[e]), ((n >> 2) - 1) & 1, a.err, abort)) break;
-        const unsigned got = atomicAdd(a.item_ctr, 1u);
+        if (n >= 4 && !warp_wait(smem_u32(&bars->it_empty[e]), ((n >> 2) - 1) & 1, a.err, abort)) break;
+        unsigned got = 0;
+        if (lane == 0) got = atomicAdd(a.item_ctr, 1u);
+        got = __shfl_sync(0xffffffffu, got, 0);
         const int it = got < static_cast<unsigned>(nitems) ? static_cast<int>(got) : -1;
-        *reinterpret_cast<volatile int*>(&bars->items[e]) = it;
-        mbar_arrive(smem_u32(&bars->it_full[e]));
+        if (lane == 0) {
+          *reinterpret_cast<volatile int*>(&bars->items[e]) = it;
+          mbar_arrive(smem_u32(&bars->it_full[e]));
+        }
+        __syncwarp();
         if (it < 0) break;
         const TcItem w = tc_item<C::NDH, BIDIR>(a, it, nqt);
         if (w.ntiles == 0) continue;
-        if (nq > 0 && !thread_wait(smem_u32(&bars->q_free), (nq - 1) & 1, a.err, abort)) break;
-        mbar_arrive_expect_tx(qb, C::QCH * kChunkB);
+        if (nq > 0 && !warp_wait(smem_u32(&bars->q_free), (nq - 1) & 1, a.err, abort)) break;
         // Q tile: 128 rows x QCH chunks in one request (two for head_dim 512)
         constexpr int QREQ = C::QCH > 4 ? 2 : 1;
+        if (elect_one()) {
+          mbar_arrive_expect_tx(qb, C::QCH * kChunkB);
 #pragma unroll
-        for (int r = 0; r < QREQ; ++r)
-          tma_load_5d(sQ + r * (C::QCH / QREQ) * kChunkB, &tm_q, 0, w.q0, r * (C::QCH / QREQ), w.h, w.b, qb);
+          for (int r = 0; r < QREQ; ++r)
+            tma_load_5d(sQ + r * (C::QCH / QREQ) * kChunkB, &tm_q, 0, w.q0, r * (C::QCH / QREQ), w.h, w.b, qb);
+        }
+        __syncwarp();
         ++nq;
         // Cache row of a key tile's first position: on a ring of max_len
         // rows (a multiple of the 128-key tile, so no tile wraps) the
@@ -318,21 +329,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto load_k = [&](int kt) {
           const int kr = tile_row(kt);
           for (int p2 = 0; p2 < C::KPARTS && ok; ++p2) {
-            if (!thread_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, a.err, abort)) { ok = false; break; }
+            if (!warp_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, a.err, abort)) { ok = false; break; }
             const uint32_t fb = smem_u32(&bars->full[slot]);
-            mbar_arrive_expect_tx(fb, C::KPB);
-            tma_load_5d(sRing + slot * C::SLOTB, &tm_k, 0, kr, p2 * C::CPP, w.kvh, w.b, fb);
+            if (elect_one()) {
+              mbar_arrive_expect_tx(fb, C::KPB);
+              tma_load_5d(sRing + slot * C::SLOTB, &tm_k, 0, kr, p2 * C::CPP, w.kvh, w.b, fb);
+            }
+            __syncwarp();
             advance();
           }
         };
         auto load_v = [&](int kt) {
           const int kr = tile_row(kt);
           for (int p2 = 0; p2 < C::VPARTS && ok; ++p2) {
-            if (!thread_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, a.err, abort)) { ok = false; break; }
+            if (!warp_wait(smem_u32(&bars->empty[slot]), phase ^ 1u, a.err, abort)) { ok = false; break; }
             const uint32_t fb = smem_u32(&bars->full[slot]);
-            mbar_arrive_expect_tx(fb, C::VPB);
-            tma_load_5d(sRing + slot * C::SLOTB, &tm_v, 0, kr + p2 * C::VKP, w.dh * (C::DV / 64), w.kvh, w.b,
-                        fb);
+            if (elect_one()) {
+              mbar_arrive_expect_tx(fb, C::VPB);
+              tma_load_5d(sRing + slot * C::SLOTB, &tm_v, 0, kr + p2 * C::VKP, w.dh * (C::DV / 64), w.kvh, w.b,
+                          fb);
+            }
+            __syncwarp();
             advance();
           }
         };
@@ -343,9 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // Copies still in flight must land before the CTA may exit.
-      if (nq > 0) thread_wait(qb, (nq - 1) & 1, nullptr);
+      if (nq > 0) warp_wait(qb, (nq - 1) & 1, nullptr);
       for (int s2 = max(0, seq - C::NSLOT); s2 < seq; ++s2)
-        thread_wait(smem_u32(&bars->full[s2 % C::NSLOT]), (s2 / C::NSLOT) & 1, nullptr);
+        warp_wait(smem_u32(&bars->full[s2 % C::NSLOT]), (s2 / C::NSLOT) & 1, nullptr);
     }
     __syncwarp();
   } else if (warp == 1) {
