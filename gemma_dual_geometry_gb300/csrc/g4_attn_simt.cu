@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(NW * 32, (SimtCfg<T, HD, G, NW>::MINB))
     for (int job = warp; job < njobs; job += NW) {
       const Job j = job_of(job);
       if (job != warp) load_job(j, f, wf);
-      norm_rope_row<T, HD, C::NPC, C::PE>(f, wf, j.src, j.w, j.rope, s_cos, s_sin, a.n_rot, a.eps, lane);
+      norm_rope_row<T, HD, C::NPC, C::PE>(f, wf, j.rope, s_cos, s_sin, a.n_rot, a.eps, lane);
       store_row<T, C::NPC, C::PE>(job < G ? s_qn + job * HD : s_kn + (job - G) * HD, lane, f);
       if (j.dst_g != nullptr) store_row<T, C::NPC, C::PE>(j.dst_g, lane, f);
     }

@@ -76,7 +76,7 @@ struct WinCfg {
   static constexpr int S_OFF = QF_OFF + G * HD * 4;        // [G][64] scores
   static constexpr int P_OFF = S_OFF + G * kWinKeys * 4;   // [64][G] probabilities
   static constexpr int ML_OFF = P_OFF + kWinKeys * G * 4;  // [G] max, [G] sum
-  static constexpr int O_OFF = ML_OFF + 2 * G * 4 + 64;    // [G][HD] partial output (read by the peers)
+  static constexpr int O_OFF = ML_OFF + (2 * G * 4 + 64 + 15) / 16 * 16;  // [G][HD] partial output (16-byte aligned)
   static constexpr int TAB_OFF = O_OFF + G * HD * 4;       // cos, sin of HD/2 pairs (double-float)
   // the cluster leader's receive area: every CTA's partial (output, max, sum)
   static constexpr int RO_OFF = TAB_OFF + HD * 8;           // [8][G][HD] f32
@@ -267,7 +267,10 @@ __global__ void __launch_bounds__(kWinThreads, (WinCfg<HD, G>::MINB))
       __syncthreads();
     }
   }
-  if (threadIdx.x == 0) {
+  // The copies are issued by the last warp, which the norm below leaves idle
+  // for G <= 5 (issuing them costs a lane several hundred cycles, which would
+  // otherwise delay that lane's warp and the norm's barrier).
+  if (warp == kWinWarps - 1 && lane == 0) {
     const uint32_t bytes = static_cast<uint32_t>(max(ncopy, 0)) * C::ROWB;
     mbar_arrive_expect_tx(smem_u32(bar), 2 * bytes);
     if (bytes > 0) {
@@ -311,8 +314,7 @@ __global__ void __launch_bounds__(kWinThreads, (WinCfg<HD, G>::MINB))
     float f[C::EL], wf[C::EL];
     for (int job = warp; job < njobs; job += kWinWarps) {
       load_job(job, f, wf);
-      norm_rope_row<T, HD, C::NPC, C::PE>(f, wf, src_of(job), w_of(job), job <= G, s_cos, s_sin, a.n_rot, a.eps,
-                                          lane);
+      norm_rope_row<T, HD, C::NPC, C::PE>(f, wf, job <= G, s_cos, s_sin, a.n_rot, a.eps, lane);
       if (job < G) {
         float g[C::EL];
 #pragma unroll
@@ -489,28 +491,39 @@ __global__ void __launch_bounds__(kWinThreads, (WinCfg<HD, G>::MINB))
       const float* ro = reinterpret_cast<const float*>(smem + C::RO_OFF);
       const float* rm = reinterpret_cast<const float*>(smem + C::RM_OFF);
       const float* rl = reinterpret_cast<const float*>(smem + C::RL_OFF);
-      // log-sum-exp weight of each (split, head), normalised: once per head
+      // log-sum-exp weight of each (split, head), normalised: all G x ns of
+      // them at once, the splits of a head on 8 consecutive lanes of warps
+      // 0-1 (ns <= 8, G <= 8), reduced with shuffles
       float* wts = s_sc;  // [ns][G] (the scores are no longer needed)
-      if (threadIdx.x < G) {
-        const int h = threadIdx.x;
-        float M = -INFINITY;
-        for (int r = 0; r < ns; ++r) M = fmaxf(M, rm[r * G + h]);
-        float den = 0.0f;
-        for (int r = 0; r < ns; ++r) {
-          const float mr = rm[r * G + h];
-          const float w = mr == -INFINITY ? 0.0f : ex2_approx(mr - M);
-          wts[r * G + h] = w;
-          den = fmaf(w, rl[r * G + h], den);
-        }
-        const float inv = den > 0.0f ? 1.0f / den : 0.0f;
-        for (int r = 0; r < ns; ++r) wts[r * G + h] *= inv;
+      static_assert(kMaxWinSplits == 8, "8 lanes per head");
+      if (threadIdx.x < 64) {
+        const int h = threadIdx.x >> 3, r = threadIdx.x & 7;
+        const bool have = h < G && r < ns;
+        const float mr = have ? rm[r * G + h] : -INFINITY;
+        float M = mr;
+#pragma unroll
+        for (int o = 4; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        const float w = mr == -INFINITY ? 0.0f : ex2_approx(mr - M);
+        float den = have ? w * rl[r * G + h] : 0.0f;
+#pragma unroll
+        for (int o = 4; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        if (have) wts[r * G + h] = den > 0.0f ? w / den : 0.0f;
       }
       __syncthreads();
-      for (int idx = threadIdx.x; idx < G * HD; idx += kWinThreads) {
+      // four consecutive outputs per thread (G x HD is a multiple of 4 and
+      // every partial is 16-byte aligned)
+      for (int idx = threadIdx.x * 4; idx < G * HD; idx += kWinThreads * 4) {
         const int h = idx / HD;
-        float val = 0.0f;
-        for (int r = 0; r < ns; ++r) val = fmaf(wts[r * G + h], ro[r * G * HD + idx], val);
-        store_elems<1>(out + idx, &val);
+        float val[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int r = 0; r < ns; ++r) {
+          const float w = wts[r * G + h];
+          const float4 x = *reinterpret_cast<const float4*>(ro + r * G * HD + idx);
+          val[0] = fmaf(w, x.x, val[0]);
+          val[1] = fmaf(w, x.y, val[1]);
+          val[2] = fmaf(w, x.z, val[2]);
+          val[3] = fmaf(w, x.w, val[3]);
+        }
+        store_elems<4>(out + idx, val);
       }
     }
   }

@@ -420,8 +420,8 @@ __device__ __forceinline__ float through(float x) {
 }
 
 // RMSNorm (optional weight) then rotate_half RoPE of one row held in the lane
-// layout above (src: the same row in memory; wf: the lane's weights, from w,
-// or ones when w is null), at position pos; the partner
+// layout above (f: the row's raw values; wf: the lane's weights, or ones for
+// a row without weight), at position pos; the partner
 // of element d is d +- HD/2, which is the same lane (NPC >= 2) or lane ^ 16
 // (NPC == 1).  bf16 results are the correctly rounded real values
 // (g4_normrope.cuh), the ones the append kernel stores, decided in three
@@ -430,8 +430,8 @@ __device__ __forceinline__ float through(float x) {
 // double-float inverse rms for the rest.  s_cos / s_sin hold cos and sin of
 // the HD/2 pairs.
 template <typename T, int HD, int NPC, int PE>
-__device__ __forceinline__ void norm_rope_row(float* f, const float* wf, const T* src, const float* w, bool rope,
-                                              const DF* s_cos, const DF* s_sin, int n_rot, float eps, int lane) {
+__device__ __forceinline__ void norm_rope_row(float* f, const float* wf, bool rope, const DF* s_cos, const DF* s_sin,
+                                              int n_rot, float eps, int lane) {
   constexpr int EL = NPC * PE;
   constexpr bool kBF16 = sizeof(T) == 2;
   constexpr float kErrY = normrope_err_y<EL>();
@@ -484,7 +484,10 @@ __device__ __forceinline__ void norm_rope_row(float* f, const float* wf, const T
   }
   if constexpr (kBF16) {
     if (__any_sync(0xffffffffu, need != 0)) {
-      // Stage 2, lane by lane, one open value per pass (operands reloaded).
+      // Stage 2, lane by lane, one open value per pass.  The operands come
+      // from the registers (a select over the lane's elements keeps the
+      // arrays in registers; reloading them from memory put an L2 round trip
+      // on every pass).
       uint32_t open = 0;
 #pragma unroll 1
       for (uint32_t left = need; left != 0; left &= left - 1) {
@@ -492,12 +495,19 @@ __device__ __forceinline__ void norm_rope_row(float* f, const float* wf, const T
         const int d = (lane + 32 * (i / PE)) * PE + i % PE;
         const bool lower = d < HD / 2;
         const int j = lower ? d : d - HD / 2;
-        const int other = lower ? d + HD / 2 : d - HD / 2;
-        const float xs = static_cast<float>(src[d]);
-        DF inner = two_prod(xs, w != nullptr ? w[d] : 1.0f);
+        float xs = 0.0f, ws = 1.0f, xo = 0.0f, wo = 1.0f;
+#pragma unroll
+        for (int k = 0; k < EL; ++k)
+          if (k == i) {
+            xs = f[k];
+            ws = wf[k];
+            xo = fp[k];
+            wo = wp[k];
+          }
+        DF inner = two_prod(xs, ws);
         float mag = fabsf(inner.h);
         if (rope && j < n_rot) {
-          const DF po = two_prod(static_cast<float>(src[other]), w != nullptr ? w[other] : 1.0f);
+          const DF po = two_prod(xo, wo);
           mag += fabsf(po.h);
           inner = df_add(df_mul(inner, s_cos[j]), df_mul(po, lower ? df_neg(s_sin[j]) : s_sin[j]));
         }
