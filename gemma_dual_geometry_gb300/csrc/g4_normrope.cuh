@@ -457,6 +457,11 @@ __device__ __forceinline__ void norm_rope_row(float* f, const float* wf, bool ro
       wp[e] = __shfl_xor_sync(0xffffffffu, wf[e], 16);
     }
   }
+  // Each element's own output only, the same float32 operations as
+  // normrope_pair_fast's output of that side (ya, yb rounded products, one
+  // fma with the partner's product; the same bounds), with the rotation's
+  // sign selected rather than branched on: with one row half per lane group
+  // (NPC == 1) a branch on the half ran both sides in every warp.
   float o[EL];
   uint32_t need = 0;
 #pragma unroll
@@ -468,18 +473,20 @@ __device__ __forceinline__ void norm_rope_row(float* f, const float* wf, bool ro
       const bool lower = d < HD / 2;
       const int j = lower ? d : d - HD / 2;
       const bool rot = rope && j < n_rot;
-      const float2 t = rot ? make_float2(s_cos[j].h, s_sin[j].h) : make_float2(1.0f, 0.0f);
-      float oa, ob;
-      bool na, nb;
-      if (lower) {
-        normrope_pair_fast(f[i], wf[i], fp[i], wp[i], r, rot, t.x, t.y, kErrY, kErrAB, kErrO, oa, ob, na, nb);
-        o[i] = oa;
-        need |= (na ? 1u : 0u) << i;
+      const float ys = (f[i] * r) * wf[i];
+      float oi, ei;
+      if (rot) {
+        const float cj = s_cos[j].h, sj = s_sin[j].h;
+        const float yo = (fp[i] * r) * wp[i];
+        const float po = yo * sj;
+        oi = fmaf(ys, cj, lower ? -po : po);
+        ei = fmaf(kErrO, fabsf(oi), kErrAB * (fabsf(ys) + fabsf(yo)));
       } else {
-        normrope_pair_fast(fp[i], wp[i], f[i], wf[i], r, rot, t.x, t.y, kErrY, kErrAB, kErrO, oa, ob, na, nb);
-        o[i] = ob;
-        need |= (nb ? 1u : 0u) << i;
+        oi = ys;
+        ei = kErrY * fabsf(ys);
       }
+      o[i] = oi;
+      need |= (fabsf(oi - bf16_midpoint(oi)) > ei ? 0u : 1u) << i;
     }
   }
   if constexpr (kBF16) {
