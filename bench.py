@@ -59,16 +59,16 @@ WIN_SOURCES = ("g4_decode_win.cu", "g4_device.cuh", "g4_internal.h", "g4_normrop
 GEMM_SOURCES = ("g4_gemm_tc.cu", "g4_device.cuh", "g4_internal.h", "g4_normrope.cuh")
 PROFILED_TRAFFIC = {
     # key: (bytes per launch, sources, digest, where it comes from)
-    "prefill_full": (523422647, PREFILL_SOURCES, "0d43a4695d5c39a2",
+    "prefill_full": (521583616, PREFILL_SOURCES, "b1c7012b5f790912",
                      "ncu launch list, 42-layer stack at batch 2, layer-5 launches, x 4 sequences"),
-    "decode_full": (134668971, DECODE_SOURCES, "1b8aa93a5cd45d12",
+    "decode_full": (134683648, DECODE_SOURCES, "9fdceb0610310b2d",
                     "ncu launch list, 42-layer stack at batch 2, full-layer decode steps, x 4 sequences"),
-    "decode_sliding": (8708935, WIN_SOURCES, "9639212a168ccbe2",
+    "decode_sliding": (8710144, WIN_SOURCES, "9196c8f8e4813a77",
                        "ncu launch list, 42-layer stack at batch 2, sliding-layer decode steps, x 4 sequences"),
-    "qkv_sliding": (299654810, GEMM_SOURCES, "9df637440ee7ed53", "ncu launch list, qkv_proj_bf16, sliding layer"),
-    "qkv_full": (513048166, GEMM_SOURCES, "9df637440ee7ed53", "ncu launch list, qkv_proj_bf16, full layer"),
-    "out_sliding": (378696346, GEMM_SOURCES, "9df637440ee7ed53", "ncu launch list, out_proj_bf16, sliding layer"),
-    "out_full": (584917094, GEMM_SOURCES, "9df637440ee7ed53", "ncu launch list, out_proj_bf16, full layer"),
+    "qkv_sliding": (299278336, GEMM_SOURCES, "542a27ab55a5fddd", "ncu launch list, qkv_proj_bf16, sliding layer"),
+    "qkv_full": (513194752, GEMM_SOURCES, "542a27ab55a5fddd", "ncu launch list, qkv_proj_bf16, full layer"),
+    "out_sliding": (378548992, GEMM_SOURCES, "542a27ab55a5fddd", "ncu launch list, out_proj_bf16, sliding layer"),
+    "out_full": (584822528, GEMM_SOURCES, "542a27ab55a5fddd", "ncu launch list, out_proj_bf16, full layer"),
 }
 
 
