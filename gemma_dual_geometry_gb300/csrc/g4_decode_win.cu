@@ -358,36 +358,39 @@ __global__ void __launch_bounds__(kWinThreads, (WinCfg<HD, G>::MINB))
     }
   bool ok = warp_wait(smem_u32(bar), 0, a.err);
   constexpr int kSh = ilog2c(C::LPK / G);
+  // All passes' partial dot products first (independent accumulators), then
+  // their reduce-scatters, so that the passes' dependency chains overlap.
+  float part_s[C::NPASS][G];
 #pragma unroll
   for (int pass = 0; pass < C::NPASS; ++pass) {
     const int key = pass * C::KPP + warp * C::KPW + lane / C::LPK;
-    float part_s[G];
+    const int kr = key < nvalid ? key : 0;  // keys past the valid ones read row 0 and are dropped below
+    float2 acc[G];
 #pragma unroll
-    for (int h = 0; h < G; ++h) part_s[h] = 0.0f;
-    if (key < nvalid) {
-      float2 acc[G];
+    for (int h = 0; h < G; ++h) acc[h] = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int h = 0; h < G; ++h) acc[h] = make_float2(0.0f, 0.0f);
+    for (int c = 0; c < C::CPL; ++c) {
+      const int pc = (c + rot) & (C::CPL - 1);
+      const uint4 kw = *reinterpret_cast<const uint4*>(sK + kr * C::ROWB + (part * C::CPL + pc) * 16);
+      const float2 k0v = make_float2(bf16_lo(kw.x), bf16_hi(kw.x));
+      const float2 k1v = make_float2(bf16_lo(kw.y), bf16_hi(kw.y));
+      const float2 k2v = make_float2(bf16_lo(kw.z), bf16_hi(kw.z));
+      const float2 k3v = make_float2(bf16_lo(kw.w), bf16_hi(kw.w));
 #pragma unroll
-      for (int c = 0; c < C::CPL; ++c) {
-        const int pc = (c + rot) & (C::CPL - 1);
-        const uint4 kw = *reinterpret_cast<const uint4*>(sK + key * C::ROWB + (part * C::CPL + pc) * 16);
-        const float2 k0v = make_float2(bf16_lo(kw.x), bf16_hi(kw.x));
-        const float2 k1v = make_float2(bf16_lo(kw.y), bf16_hi(kw.y));
-        const float2 k2v = make_float2(bf16_lo(kw.z), bf16_hi(kw.z));
-        const float2 k3v = make_float2(bf16_lo(kw.w), bf16_hi(kw.w));
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          acc[h] = fma2w(qr[h][c][0], k0v, acc[h]);
-          acc[h] = fma2w(qr[h][c][1], k1v, acc[h]);
-          acc[h] = fma2w(qr[h][c][2], k2v, acc[h]);
-          acc[h] = fma2w(qr[h][c][3], k3v, acc[h]);
-        }
+      for (int h = 0; h < G; ++h) {
+        acc[h] = fma2w(qr[h][c][0], k0v, acc[h]);
+        acc[h] = fma2w(qr[h][c][1], k1v, acc[h]);
+        acc[h] = fma2w(qr[h][c][2], k2v, acc[h]);
+        acc[h] = fma2w(qr[h][c][3], k3v, acc[h]);
       }
-#pragma unroll
-      for (int h = 0; h < G; ++h) part_s[h] = acc[h].x + acc[h].y;
     }
-    const float sc = group_reduce_scatter<G, C::LPK>(part_s, lane);
+#pragma unroll
+    for (int h = 0; h < G; ++h) part_s[pass][h] = key < nvalid ? acc[h].x + acc[h].y : 0.0f;
+  }
+#pragma unroll
+  for (int pass = 0; pass < C::NPASS; ++pass) {
+    const int key = pass * C::KPP + warp * C::KPW + lane / C::LPK;
+    const float sc = group_reduce_scatter<G, C::LPK>(part_s[pass], lane);
     if ((part & ((1 << kSh) - 1)) == 0) s_sc[(part >> kSh) * kWinKeys + key] = sc;
   }
   __syncthreads();
@@ -422,12 +425,13 @@ __global__ void __launch_bounds__(kWinThreads, (WinCfg<HD, G>::MINB))
   {
     const int dp = threadIdx.x % C::NDP;
     const int ks = threadIdx.x / C::NDP;
-    // every key of the slice, unrolled, two accumulator sets (even / odd
-    // keys); keys past this CTA's valid ones read nothing (their rows may
-    // hold anything, and their probabilities are zero)
-    float2 acc[2][G];
+    // every key of the slice, unrolled, four accumulator sets (key index mod
+    // 4); keys past this CTA's valid ones read nothing (their rows may hold
+    // anything, and their probabilities are zero)
+    constexpr int NA = C::KPS >= 4 ? 4 : C::KPS;  // accumulator sets (keys kk mod NA)
+    float2 acc[NA][G];
 #pragma unroll
-    for (int u = 0; u < 2; ++u)
+    for (int u = 0; u < NA; ++u)
 #pragma unroll
       for (int h = 0; h < G; ++h) acc[u][h] = make_float2(0.0f, 0.0f);
 #pragma unroll
@@ -447,11 +451,15 @@ __global__ void __launch_bounds__(kWinThreads, (WinCfg<HD, G>::MINB))
         for (int h = 0; h < G; ++h) pk[h] = s_p[key * G + h];
       }
 #pragma unroll
-      for (int h = 0; h < G; ++h) acc[kk & 1][h] = fma2w(make_float2(pk[h], pk[h]), vv, acc[kk & 1][h]);
+      for (int h = 0; h < G; ++h) acc[kk % NA][h] = fma2w(make_float2(pk[h], pk[h]), vv, acc[kk % NA][h]);
     }
     float2 accs[G];
 #pragma unroll
-    for (int h = 0; h < G; ++h) accs[h] = make_float2(acc[0][h].x + acc[1][h].x, acc[0][h].y + acc[1][h].y);
+    for (int h = 0; h < G; ++h) {
+      accs[h] = acc[0][h];
+#pragma unroll
+      for (int u = 1; u < NA; ++u) accs[h] = make_float2(accs[h].x + acc[u][h].x, accs[h].y + acc[u][h].y);
+    }
     __syncthreads();  // every K / V read is done: the area takes the slice sums
     float2* red = reinterpret_cast<float2*>(smem);  // [NKS][G][HD/2]
 #pragma unroll
