@@ -63,7 +63,7 @@ PROFILED_TRAFFIC = {
                      "ncu launch list, 42-layer stack at batch 2, layer-5 launches, x 4 sequences"),
     "decode_full": (134683648, DECODE_SOURCES, "9fdceb0610310b2d",
                     "ncu launch list, 42-layer stack at batch 2, full-layer decode steps, x 4 sequences"),
-    "decode_sliding": (8710144, WIN_SOURCES, "9196c8f8e4813a77",
+    "decode_sliding": (8710144, WIN_SOURCES, "b2ca64d9b97a6cb4",
                        "ncu launch list, 42-layer stack at batch 2, sliding-layer decode steps, x 4 sequences"),
     "qkv_sliding": (299278336, GEMM_SOURCES, "542a27ab55a5fddd", "ncu launch list, qkv_proj_bf16, sliding layer"),
     "qkv_full": (513194752, GEMM_SOURCES, "542a27ab55a5fddd", "ncu launch list, qkv_proj_bf16, full layer"),
